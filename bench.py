@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the decode-step selective state update on one GB300 (or N replicas).
+
+A step is one ``ssu_update`` call: one decode step of every request in the batch, all heads
+(index gather, dt/dA, state load, update and in-place store, readout).  The default
+workload is the serving decode batch: 128 requests, 16 heads, headdim 64, dstate 128, fp32
+state, bf16 x/B/C, over a 2432-slot pool split into 19 disjoint 128-slot sets.
+
+Timing follows the kernel measurement of sglang PR #41223 (Details / Kernel measurement):
+the calls are captured in CUDA graphs, call i touches slot set (i mod K), and the K sets
+together hold at least 3x the L2, so every call reads its state from HBM.  The K timed
+steps are bracketed by CUDA events on the launching stream; the reported value is the
+time per call (lower is better).  Batches 8 and 512 are measured the same way and reported
+under ``by_batch``.
+
+``--impl reference`` times the double-precision CPU oracle instead (the reference arm):
+the same metric and workload, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+
+METRIC = "µs/call and achieved HBM TB/s (% of peak), H=16 at batch 8/128/512, cold L2"
+UNIT = "us/call"
+NHEADS, HEADDIM, DSTATE, NGROUPS = 16, 64, 128, 1
+DEFAULT_BATCH = 128
+SERVING_SETS = 19            # 2432 slots at batch 128
+NOMINAL_HBM_GBS = 8000.0     # the pages' round GB200/B200 HBM3e figure
+FALLBACK_HBM_GBS = 6800.0
+PAGE_US = {8: 4.02, 128: 24.1, 512: 85.7}   # sglang PR #41223 Speedup Result, B200 (context)
+KERNEL_SOURCE = ROOT / "selective_state_update_02_gb300" / "csrc" / "ssu.cu"
+
+
+# ---- arithmetic of the measurement (host logic, tested on CPU) ---------------------------
+
+def bytes_per_call(bs: int, H: int = NHEADS, P: int = HEADDIM, N: int = DSTATE,
+                   G: int = NGROUPS, idx_bytes: int = 4) -> int:
+    """Algorithmic HBM bytes of one call: the state read and written once, every input read
+    once, the output written once; per-head parameters counted once (stride-0 broadcasts)."""
+    state = 2 * bs * H * P * N * 4
+    x = bs * H * P * 2
+    y = bs * H * P * 2
+    bc = 2 * bs * G * N * 2
+    dt = bs * H * 2
+    idx = bs * idx_bytes
+    params = 3 * H * 4
+    return state + x + y + bc + dt + idx + params
+
+
+def flops_per_call(bs: int, H: int = NHEADS, P: int = HEADDIM, N: int = DSTATE) -> int:
+    """Update (multiply + fma) and readout (fma) per state element."""
+    return 5 * bs * H * P * N
+
+
+def sets_for(bs: int, H: int, l2_bytes: int) -> int:
+    import workloads as wl
+    if bs == DEFAULT_BATCH and H == NHEADS:
+        return max(SERVING_SETS, wl.sets_for_cold_l2(bs, H, l2_bytes))
+    return wl.sets_for_cold_l2(bs, H, l2_bytes)
+
+
+def load_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def source_digest() -> str:
+    return hashlib.sha256(KERNEL_SOURCE.read_bytes()).hexdigest()[:16]
+
+
+def recorded_traffic(workload_tag: str) -> int | None:
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source.
+
+    The summaries under profiles/ carry a line
+    ``traffic_per_launch_bytes: <int> source: <digest> workload: <tag>``.
+    """
+    digest = source_digest()
+    for f in sorted((ROOT / "profiles").glob("*.md")):
+        for m in re.finditer(r"traffic_per_launch_bytes:\s*(\d+)\s+source:\s*([0-9a-f]+)\s+"
+                             r"workload:\s*(\S+)", f.read_text()):
+            if m.group(2) == digest and m.group(3) == workload_tag:
+                return int(m.group(1))
+    return None
+
+
+def aggregate_value(elapsed_us_per_rank: list[float], steps: int) -> float:
+    """Whole-job time per call: the slowest rank's time over every rank's calls."""
+    return max(elapsed_us_per_rank) / (steps * len(elapsed_us_per_rank))
+
+
+def gather_elapsed(elapsed_us: float, world: int, device) -> list[float]:
+    """Every rank's timed-region length (µs), gathered on every rank (no data-path
+    collective: this is the only exchange, after the timed region)."""
+    if world <= 1:
+        return [elapsed_us]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_us], dtype=torch.float64, device=device)
+    parts = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(parts, t)
+    return [float(v.item()) for v in parts]
+
+
+def parse_clocks(csv_text: str) -> dict | None:
+    rows = []
+    for line in csv_text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9 or not parts[0].isdigit():
+            continue
+        try:
+            sm = float(parts[1].split()[0])
+            smax = float(parts[2].split()[0])
+            power = float(parts[3].split()[0])
+        except ValueError:
+            continue
+        rows.append((sm, smax, power, parts[5:9]))
+    if not rows:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+    loaded = [r[0] for r in rows if r[2] > 200.0] or [r[0] for r in rows]
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows)}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.text, _ = self.proc.communicate()
+        return False
+
+    def result(self):
+        return parse_clocks(getattr(self, "text", ""))
+
+
+# ---- the GPU arm --------------------------------------------------------------------------
+
+class Workload:
+    """Device-resident rotation workload for one batch size."""
+
+    def __init__(self, bs: int, H: int, dev, seed: int, l2_bytes: int, packed: bool = False):
+        import torch
+
+        import selective_state_update_02_gb300 as ssu
+        import workloads as wl
+        self.bs, self.H = bs, H
+        self.n_sets = sets_for(bs, H, l2_bytes)
+        rng = np.random.default_rng(seed)
+        pool = wl.state_pool(rng, bs * self.n_sets, H)
+        self.pool = torch.from_numpy(pool).to(dev)
+        del pool
+        self.sets = torch.from_numpy(wl.rotation_sets(bs, self.n_sets, seed).astype(np.int32)) \
+            .to(dev)
+        dt_bias, A, D = wl.head_params(rng, H)
+        self.dt_bias = torch.from_numpy(dt_bias).to(dev).unsqueeze(-1).expand(H, HEADDIM)
+        self.A = torch.from_numpy(A).to(dev)[:, None, None].expand(H, HEADDIM, DSTATE)
+        self.D = torch.from_numpy(D).to(dev).unsqueeze(-1).expand(H, HEADDIM)
+        # per set: x, B, C as strided views of one packed bf16 tensor, dt head-expanded
+        width = H * HEADDIM + 2 * NGROUPS * DSTATE
+        self.packed = torch.from_numpy(
+            wl.packed_xbc(rng, bs * self.n_sets, H).view(np.int16)).view(torch.bfloat16) \
+            .to(dev).view(self.n_sets, bs, width)
+        self.dt = torch.from_numpy(wl.f32_to_bf16_bits(
+            rng.uniform(-4, 0, (self.n_sets, bs, H)).astype(np.float32)).view(np.int16)) \
+            .view(torch.bfloat16).to(dev)
+        self.out = torch.zeros(self.n_sets, bs, H, HEADDIM, dtype=torch.bfloat16, device=dev)
+        self.args = []
+        for k in range(self.n_sets):
+            pk = self.packed[k]
+            x = pk[:, :H * HEADDIM].view(bs, H, HEADDIM)
+            B = pk[:, H * HEADDIM:H * HEADDIM + DSTATE].unsqueeze(1)
+            C = pk[:, H * HEADDIM + DSTATE:].unsqueeze(1)
+            dt = self.dt[k].unsqueeze(-1).expand(bs, H, HEADDIM)
+            tensors = (self.pool, self.sets[k], x, dt, self.dt_bias, self.A, B, C, self.D,
+                       self.out[k])
+            shape, strides = ssu.describe(*tensors)
+            self.args.append(([t.data_ptr() for t in tensors], shape, strides))
+        self.packed_layout = packed
+
+    def call(self, handle, i: int, stream_ptr: int) -> None:
+        import selective_state_update_02_gb300 as ssu
+        ptrs, shape, strides = self.args[i % self.n_sets]
+        st = ssu.ssu_update_raw(handle, ptrs, shape, strides, stream_ptr)
+        if st != 0:
+            raise ssu.SsuError(st, "ssu_update", ssu.last_error())
+
+
+def time_calls(wl_, handle, steps: int, warmup: int, clocks_gpu: int | None = None):
+    """Warm up, then time exactly `steps` calls replayed from CUDA graphs.
+
+    Returns (elapsed_ms, untimed_calls, clocks).
+    """
+    import torch
+    stream = torch.cuda.Stream()
+    per_graph = wl_.n_sets * max(1, math.ceil(200 / wl_.n_sets))
+    per_graph = min(per_graph, max(steps, 1))
+    full, rem = divmod(steps, per_graph)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            wl_.call(handle, i, stream.cuda_stream)
+    stream.synchronize()
+    graphs = []
+    for n in ([per_graph] if full else []) + ([rem] if rem else []):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            cur = torch.cuda.current_stream().cuda_stream
+            for i in range(n):
+                wl_.call(handle, i, cur)
+        graphs.append((g, n))
+    # one untimed replay of each graph (uploads it and warms the launch path)
+    untimed = warmup
+    with torch.cuda.stream(stream):
+        for g, n in graphs:
+            g.replay()
+            untimed += n
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(clocks_gpu) if clocks_gpu is not None else None
+    if sampler:
+        sampler.__enter__()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        if full:
+            g, _ = graphs[0]
+            for _ in range(full):
+                g.replay()
+        if rem:
+            graphs[-1][0].replay()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    clocks = None
+    if sampler:
+        sampler.__exit__(None, None, None)
+        clocks = sampler.result()
+    return ev0.elapsed_time(ev1), untimed, clocks
+
+
+def time_e2e(wl_, handle, steps: int, dev) -> dict:
+    """Public-API path with host buffers: per step, one pinned host->device copy of the
+    step's inputs (indices, x/B/C, dt), the update, one device->host copy of the output."""
+    import torch
+
+    import selective_state_update_02_gb300 as ssu
+    bs, H = wl_.bs, wl_.H
+    width = H * HEADDIM + 2 * DSTATE
+    # one pinned staging buffer per step input set: [idx int32 | packed x/B/C | dt] as bytes
+    n_idx, n_xbc, n_dt = bs * 4, bs * width * 2, bs * H * 2
+    step_bytes = n_idx + n_xbc + n_dt
+    host_in = torch.empty(wl_.n_sets, step_bytes, dtype=torch.uint8, pin_memory=True)
+    for k in range(wl_.n_sets):
+        host_in[k, :n_idx].copy_(wl_.sets[k].cpu().view(torch.uint8))
+        host_in[k, n_idx:n_idx + n_xbc].copy_(wl_.packed[k].cpu().reshape(-1).view(torch.uint8))
+        host_in[k, n_idx + n_xbc:].copy_(wl_.dt[k].cpu().reshape(-1).view(torch.uint8))
+    dev_in = torch.empty(step_bytes, dtype=torch.uint8, device=dev)
+    idx = dev_in[:n_idx].view(torch.int32)
+    pk = dev_in[n_idx:n_idx + n_xbc].view(torch.bfloat16).view(bs, width)
+    dt = dev_in[n_idx + n_xbc:].view(torch.bfloat16).view(bs, H).unsqueeze(-1) \
+        .expand(bs, H, HEADDIM)
+    x = pk[:, :H * HEADDIM].view(bs, H, HEADDIM)
+    B = pk[:, H * HEADDIM:H * HEADDIM + DSTATE].unsqueeze(1)
+    C = pk[:, H * HEADDIM + DSTATE:].unsqueeze(1)
+    out = torch.empty(bs, H, HEADDIM, dtype=torch.bfloat16, device=dev)
+    host_out = torch.empty(wl_.n_sets, bs, H, HEADDIM, dtype=torch.bfloat16, pin_memory=True)
+    stream = torch.cuda.Stream()
+
+    def step(k):
+        dev_in.copy_(host_in[k], non_blocking=True)
+        ssu.ssu_update(handle, wl_.pool, idx, x, dt, wl_.dt_bias, wl_.A, B, C, wl_.D, out,
+                       stream)
+        host_out[k].copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            step(i % wl_.n_sets)
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(steps):
+            step(i % wl_.n_sets)
+        ev1.record(stream)
+    stream.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    return {"value": round(ms * 1000.0 / steps, 3), "unit": UNIT, "steps": steps,
+            "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": bs * H * HEADDIM * 2,
+            "path": "binding ssu_update (C ABI) per step, pinned host buffers, eager"}
+
+
+# ---- the oracle on the host cores -----------------------------------------------------------
+
+class OracleCall:
+    """One decode step of the batch run by the double-precision oracle on the host cores."""
+
+    def __init__(self, bs: int, H: int, seed: int):
+        import oracle
+        import workloads as wl
+        oracle.build()
+        self.oracle = oracle
+        rng = np.random.default_rng(seed)
+        # the call's own slots: a pool of bs slots addressed by a random permutation
+        self.pool0 = wl.state_pool(rng, bs, H).astype(np.float64)
+        self.idx = rng.permutation(bs).astype(np.int64)
+        self.dt_bias, self.A, self.D = wl.head_params(rng, H)
+        self.x, self.dt, self.B, self.C = wl.request_inputs(rng, bs, H)
+        self.bs = bs
+        self.threads = os.cpu_count() or 1
+
+    def run(self, requests: int | None = None) -> float:
+        """Seconds for one call over the first `requests` requests (all by default)."""
+        n = self.bs if requests is None else max(1, min(self.bs, requests))
+        pool = self.pool0.copy()
+        t0 = time.perf_counter()
+        self.oracle.ssu_step_inplace(pool, self.idx[:n], self.x[:n], self.dt[:n], self.dt_bias,
+                                     self.A, self.B[:n], self.C[:n], self.D,
+                                     threads=self.threads)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(bs: int, H: int, budget_s: float = 12.0) -> dict:
+    oc = OracleCall(bs, H, seed=7)
+    oc.run()
+    times = []
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s and len(times) < 50:
+        times.append(oc.run())
+    med = statistics.median(times)
+    return {"value": round(med * 1e6, 1), "unit": UNIT, "cores": oc.threads, "kind": "oracle",
+            "sample": f"{len(times)} full calls (batch {bs}, {H} heads, headdim 64, dstate 128) "
+                      f"of the fp64 C oracle split over {oc.threads} host threads; median"}
+
+
+# ---- main ---------------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    bs, H = args.batch, NHEADS
+    oc = OracleCall(bs, H, seed=7)
+    t_full = min(oc.run() for _ in range(2))
+    budget = 120.0
+    total = args.steps + args.warmup
+    req = max(1, min(bs, int(bs * budget / max(total * t_full, 1e-9))))
+    for _ in range(args.warmup):
+        oc.run(req)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oc.run(req)
+    per_step = (time.perf_counter() - t0) / args.steps
+    value = per_step * (bs / req) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1000.0, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_for(bs, sets_for(bs, H, 126 * 2 ** 20)),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oc.threads,
+                         "kind": "oracle",
+                         "sample": f"each step: the fp64 C oracle on {req} of {bs} requests "
+                                   f"({H} heads) over {oc.threads} host threads, scaled to the "
+                                   f"full batch"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_for(bs: int, n_sets: int) -> dict:
+    return {"workload": f"decode step, batch {bs}, {NHEADS} heads, headdim {HEADDIM}, dstate "
+                        f"{DSTATE}, fp32 state pool of {bs * n_sets} slots in {n_sets} disjoint "
+                        f"{bs}-slot rotation sets; x/B/C strided views of one packed bf16 "
+                        f"tensor, dt/A/D/dt_bias stride-0 broadcasts",
+            "batch": bs, "nheads": NHEADS, "headdim": HEADDIM, "dstate": DSTATE,
+            "ngroups": NGROUPS, "pool_slots": bs * n_sets,
+            "l2": f"inputs larger than L2: call i touches set i mod {n_sets}; the sets hold "
+                  f"{bs * n_sets * NHEADS * HEADDIM * DSTATE * 4 / 2 ** 20:.0f} MiB of state"}
+
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import selective_state_update_02_gb300 as ssu
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the kernels have no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    ssu.lib()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = ssu.ssu_create(local)
+    warmup = max(args.warmup, 3)
+    bs = args.batch
+    main = Workload(bs, NHEADS, dev, seed=rank, l2_bytes=l2, packed=True)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    ms, untimed, clocks = time_calls(main, handle, args.steps, warmup, clocks_gpu=_smi_index(local))
+    barrier()
+    per_rank = gather_elapsed(ms * 1000.0, world, dev)
+    value = aggregate_value(per_rank, args.steps)
+    per_launch_us = max(per_rank) / args.steps
+    peaks = load_peaks()
+    bpc = bytes_per_call(bs)
+    achieved_gbs = bpc / (per_launch_us * 1e-6) / 1e9
+    tag = f"batch{bs}"
+    traffic = recorded_traffic(tag)
+    launch = ssu.ssu_get_launch(handle, main.args[0][1])
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": untimed, "ms_per_step": round(value / 1000.0, 6),
+        "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": round(value / PAGE_US[bs], 4) if bs in PAGE_US and world == 1 else None,
+        "vs_baseline_note": "value / the pages' B200 Triton time for this batch (another "
+                            "machine: context, not the target)",
+        "dtype": "f32", "data": "synthetic",
+        "config": config_for(bs, main.n_sets) | {
+            "launch": {"mode": launch[0], "rows_per_warp": launch[1],
+                       "warps_per_cta": launch[2], "stages": launch[3]}},
+        "achieved_tbps": round(achieved_gbs / 1000.0, 3),
+        "pct_of_nominal_8tbps": round(100.0 * achieved_gbs / NOMINAL_HBM_GBS, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": bpc,
+                     "peak_source": peaks["source"], "kernel": "ssu_vec_kernel"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.skip_extra and world == 1:
+        by = {}
+        for b in (8, 128, 512):
+            if b == bs:
+                by[str(b)] = {"us_per_call": round(per_launch_us, 3),
+                              "tbps": round(achieved_gbs / 1000.0, 3)}
+                continue
+            w = Workload(b, NHEADS, dev, seed=100 + b, l2_bytes=l2)
+            n = max(2000, min(args.steps, int(2e5 / max(b, 1))))
+            ms_b, _, _ = time_calls(w, handle, n, warmup)
+            us = ms_b * 1000.0 / n
+            by[str(b)] = {"us_per_call": round(us, 3),
+                          "tbps": round(bytes_per_call(b) / (us * 1e-6) / 1e12, 3),
+                          "pages_b200_us": PAGE_US[b], "steps": n}
+            del w
+            torch.cuda.empty_cache()
+        line["by_batch"] = by
+    if not args.skip_e2e:
+        line["e2e"] = time_e2e(main, handle, min(args.steps, args.e2e_steps), dev)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(bs, NHEADS)
+    ssu.ssu_destroy(handle)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _smi_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [p for p in vis.split(",") if p.strip()]
+        if local < len(parts) and parts[local].strip().isdigit():
+            return int(parts[local])
+    return local
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=DEFAULT_BATCH, choices=[8, 128, 512])
+    ap.add_argument("--e2e-steps", type=int, default=5000)
+    ap.add_argument("--skip-extra", action="store_true", help="skip the batch 8/512 lines")
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.steps < 1:
+        raise SystemExit("--steps must be >= 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * ssu.h - C ABI of the GB300 (sm_103a) Mamba2 decode-step selective state update.
+ *
+ * The operation (operands as in sglang PR #41223, Summary and Details / Kernel measurement:
+ * "each step it reads and writes every request's fp32 SSM state"; state pool
+ * [pool, H, 64, 128] fp32 with random state_batch_indices; x [bs, H, 64] and B/C [bs, 1, 128]
+ * as strided views of one tensor; dt, A, D and dt_bias as stride-0 broadcasts).  The pages
+ * never print the arithmetic; this library computes the standard Mamba2 decode step:
+ *
+ *   for each request b (slot s = state_batch_indices[b]) and head h (group g = h / (H/G)):
+ *     dtv      = softplus(dt[b,h] + dt_bias[h])            fp32
+ *     dA       = exp(dtv * A[h])                           fp32
+ *     S[p,n]   = S[p,n] * dA + (dtv * x[b,h,p]) * B[b,g,n]  in place in state_pool[s,h]
+ *     out[b,h,p] = bf16_rne( sum_n S[p,n] * C[b,g,n] + D[h] * x[b,h,p] )
+ *
+ * Types.  The state pool is fp32.  x, dt, B, C and out are bfloat16, passed as uint16_t
+ * pointers to their bit patterns.  dt_bias, A and D are fp32.  state_batch_indices is int32
+ * or int64 (ssu_shape_t.index_dtype).  All data pointers are DEVICE pointers on the handle's
+ * device; the caller owns every buffer.  Sizes and strides are in ELEMENTS (not bytes).
+ *
+ * Streams and asynchrony.  ssu_update validates on the host, then enqueues one kernel on
+ * `stream` and returns.  It allocates nothing, copies nothing and never synchronises, so it
+ * may be captured in a CUDA graph.  ssu_get_error is the only call that synchronises.
+ *
+ * Errors.  Every entry point returns an ssu_status_t.  Argument errors are detected on the
+ * host before anything is enqueued; ssu_last_error() then holds a one-line explanation
+ * (thread-local).  A request whose slot lies outside [0, pool_size) is skipped on the device
+ * (its slot and its out rows are not touched) and counted; ssu_get_error reports the count.
+ * Duplicate slots within one call are a precondition violation (two requests would update
+ * the same state concurrently); they are not detected.
+ *
+ * Threading.  A handle may be used from one host thread at a time.  Calls on different
+ * handles are independent.
+ */
+#ifndef SSU_H
+#define SSU_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSU_ABI_VERSION 1
+
+/* Opaque per-device context: holds the device error counters and the launch-shape choice. */
+typedef struct ssu_handle_s *ssu_handle_t;
+
+/* The same type as cudaStream_t.  NULL means the legacy default stream. */
+typedef struct CUstream_st *ssu_stream_t;
+
+typedef enum {
+    SSU_OK = 0,
+    SSU_ERR_INVALID_ARG = 1, /* NULL pointer or handle, negative size, H % G != 0, bad stride */
+    SSU_ERR_UNSUPPORTED = 2, /* a size or stride form this build does not implement */
+    SSU_ERR_MISALIGNED = 3,  /* state_pool base or a state stride not a multiple of 16 bytes */
+    SSU_ERR_CUDA = 4,        /* a CUDA runtime call failed; ssu_last_error() names it */
+    SSU_ERR_INDEX_OOB = 5    /* ssu_get_error: at least one request was skipped */
+} ssu_status_t;
+
+typedef enum { SSU_INDEX_I32 = 0, SSU_INDEX_I64 = 1 } ssu_index_dtype_t;
+
+/* Problem sizes of one call. */
+typedef struct {
+    int64_t batch;       /* bs: requests in this step; 0 is valid and enqueues nothing */
+    int64_t nheads;      /* H >= 1 */
+    int64_t headdim;     /* P >= 1 */
+    int64_t dstate;      /* N: this build implements N = 128 */
+    int64_t ngroups;     /* G >= 1 with H % G == 0; head h reads group h / (H / G) */
+    int64_t pool_size;   /* slots in state_pool; valid slot ids are [0, pool_size) */
+    int32_t index_dtype; /* ssu_index_dtype_t of state_batch_indices */
+    int32_t reserved;    /* set to 0 */
+} ssu_shape_t;
+
+/*
+ * Element strides of every operand, outermost dimension first.  Broadcast operands carry the
+ * expanded shapes that the model uses ("head-expanded"), with stride 0 over the expanded
+ * dimensions; any non-negative outer stride is accepted.
+ */
+typedef struct {
+    int64_t state[4];   /* state_pool [pool, H, P, N]: N-stride must be 1; the other three
+                           must be multiples of 4 (16-byte rows) */
+    int64_t x[3];       /* x   [bs, H, P]: P-stride must be 1 */
+    int64_t out[3];     /* out [bs, H, P]: P-stride must be 1 */
+    int64_t dt[3];      /* dt  [bs, H, P]: P-stride must be 0 (one value per head) */
+    int64_t B[3];       /* B   [bs, G, N]: N-stride must be 1 */
+    int64_t C[3];       /* C   [bs, G, N]: N-stride must be 1 */
+    int64_t dt_bias[2]; /* dt_bias [H, P]: P-stride must be 0 */
+    int64_t D[2];       /* D       [H, P]: P-stride must be 0 */
+    int64_t A[3];       /* A       [H, P, N]: P- and N-strides must be 0 */
+    int64_t idx;        /* state_batch_indices [bs] */
+} ssu_strides_t;
+
+/* Launch shapes of the streaming kernel. */
+typedef enum {
+    SSU_MODE_AUTO = 0,   /* use the built-in table (the default) */
+    SSU_MODE_VEC = 1,    /* 16-byte vector loads and stores straight from registers */
+    SSU_MODE_BULK = 2    /* bulk asynchronous copies through shared memory */
+} ssu_mode_t;
+
+typedef struct {
+    int32_t mode;          /* ssu_mode_t */
+    int32_t rows_per_warp; /* VEC: state rows (of N floats) one warp streams: 1,2,4,8,16 */
+    int32_t warps_per_cta; /* VEC: 1..16; BULK: compute warps per CTA, 1..16 */
+    int32_t stages;        /* BULK: shared-memory pipeline depth, 2..8; VEC: ignored */
+} ssu_launch_t;
+
+/* ABI version this library was built with (SSU_ABI_VERSION). */
+int32_t ssu_abi_version(void);
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *ssu_status_string(ssu_status_t status);
+
+/* One-line explanation of the last error returned on this host thread ("" if none). */
+const char *ssu_last_error(void);
+
+/*
+ * Create a handle on CUDA device `device`.  Allocates 16 bytes of device memory for the
+ * skipped-request counters and queries the SM count.  Returns SSU_ERR_CUDA without a
+ * usable device.  *out is set only on success.
+ */
+ssu_status_t ssu_create(ssu_handle_t *out, int32_t device);
+
+/* Release the handle and its device memory.  NULL is accepted.  Work enqueued earlier on
+ * its streams must have finished (the counters are freed). */
+ssu_status_t ssu_destroy(ssu_handle_t handle);
+
+/*
+ * Host-side validation of one call, exactly as ssu_update performs it, without a handle or a
+ * device: pointers are checked for NULL and alignment only, never dereferenced.
+ */
+ssu_status_t ssu_validate(const float *state_pool, const void *state_batch_indices,
+                          const uint16_t *x, const uint16_t *dt, const float *dt_bias,
+                          const float *A, const uint16_t *B, const uint16_t *C, const float *D,
+                          const uint16_t *out, const ssu_shape_t *shape,
+                          const ssu_strides_t *strides);
+
+/*
+ * One decode step.  Reads x, dt, dt_bias, A, B, C, D and the state of every slot in
+ * state_batch_indices; writes the updated state back to the same slot and the readout to
+ * out.  Enqueued on `stream`; returns once enqueued.  Slots that no request names are never
+ * read or written.  See the file header for the arithmetic and the error behaviour.
+ */
+ssu_status_t ssu_update(ssu_handle_t handle, float *state_pool, const void *state_batch_indices,
+                        const uint16_t *x, const uint16_t *dt, const float *dt_bias,
+                        const float *A, const uint16_t *B, const uint16_t *C, const float *D,
+                        uint16_t *out, const ssu_shape_t *shape, const ssu_strides_t *strides,
+                        ssu_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the handle's skipped-request counters.
+ * *skipped receives the number of requests skipped since the last read (may be NULL);
+ * *first_bad receives the smallest skipped request index b, or -1 (may be NULL).
+ * Returns SSU_ERR_INDEX_OOB when *skipped > 0, SSU_OK otherwise.
+ */
+ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *skipped,
+                           int64_t *first_bad);
+
+/*
+ * Force a launch shape for later ssu_update calls on this handle (for sweeps and tests).
+ * NULL, or mode SSU_MODE_AUTO, restores the built-in table.  Every accepted shape computes
+ * bit-identical results: each row's readout is summed in one fixed order.
+ */
+ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch);
+
+/* The launch shape ssu_update would use for `shape` on this handle (table or override). */
+ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
+                            ssu_launch_t *launch);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSU_H */

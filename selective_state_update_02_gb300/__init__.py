@@ -1,0 +1,299 @@
+"""GB300 (sm_103a) Mamba2 decode-step selective state update.
+
+Python binding of ``libssu.so`` (C ABI declared in ``include/ssu.h``).  The functions carry
+the C names and only marshal arguments: tensor pointers, sizes and element strides go into
+the ABI structs, and every step of the update runs in the library's CUDA kernels.  There is
+no CPU or PyTorch fallback: if the library is missing, every entry point raises.
+
+Operand layout (sglang PR #41223, Details / Kernel measurement): ``state_pool`` fp32
+``[pool, H, P, N]``; ``state_batch_indices`` int32/int64 ``[bs]``; ``x`` and ``out`` bf16
+``[bs, H, P]``; ``B`` and ``C`` bf16 ``[bs, G, N]``; ``dt`` bf16 ``[bs, H]`` (or the
+head-expanded ``[bs, H, P]`` view with stride 0 over P); ``dt_bias`` and ``D`` fp32 ``[H]``
+(or ``[H, P]`` with stride 0); ``A`` fp32 ``[H]`` (or ``[H, P, N]`` with strides 0).
+Strided views are accepted as they are; nothing is copied.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libssu.so"
+
+SSU_OK = 0
+SSU_ERR_INVALID_ARG = 1
+SSU_ERR_UNSUPPORTED = 2
+SSU_ERR_MISALIGNED = 3
+SSU_ERR_CUDA = 4
+SSU_ERR_INDEX_OOB = 5
+
+SSU_INDEX_I32 = 0
+SSU_INDEX_I64 = 1
+
+SSU_MODE_AUTO = 0
+SSU_MODE_VEC = 1
+SSU_MODE_BULK = 2
+
+_i64 = ctypes.c_int64
+
+
+class ssu_shape_t(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("nheads", _i64), ("headdim", _i64), ("dstate", _i64),
+                ("ngroups", _i64), ("pool_size", _i64), ("index_dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class ssu_strides_t(ctypes.Structure):
+    _fields_ = [("state", _i64 * 4), ("x", _i64 * 3), ("out", _i64 * 3), ("dt", _i64 * 3),
+                ("B", _i64 * 3), ("C", _i64 * 3), ("dt_bias", _i64 * 2), ("D", _i64 * 2),
+                ("A", _i64 * 3), ("idx", _i64)]
+
+
+class ssu_launch_t(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
+
+
+class SsuError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}: {message}")
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_EXPORTS = {
+    "ssu_abi_version": (ctypes.c_int32, []),
+    "ssu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "ssu_last_error": (ctypes.c_char_p, []),
+    "ssu_create": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.c_int32]),
+    "ssu_destroy": (ctypes.c_int, [_vp]),
+    "ssu_validate": (ctypes.c_int, [_vp] * 10 + [ctypes.POINTER(ssu_shape_t),
+                                                 ctypes.POINTER(ssu_strides_t)]),
+    "ssu_update": (ctypes.c_int, [_vp] * 11 + [ctypes.POINTER(ssu_shape_t),
+                                               ctypes.POINTER(ssu_strides_t), _vp]),
+    "ssu_get_error": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32),
+                                     ctypes.POINTER(ctypes.c_int64)]),
+    "ssu_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_launch_t)]),
+    "ssu_get_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_shape_t),
+                                      ctypes.POINTER(ssu_launch_t)]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        handle = ctypes.CDLL(str(LIB_PATH))
+        for name, (res, args) in _EXPORTS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        if handle.ssu_abi_version() != 1:
+            raise RuntimeError("libssu.so ABI version mismatch")
+        _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ssu_status_string(status).decode()
+
+
+def last_error() -> str:
+    return lib().ssu_last_error().decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != SSU_OK:
+        raise SsuError(status, where, last_error())
+
+
+# ---- marshalling -------------------------------------------------------------------------
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _expect(t: torch.Tensor, name: str, dtype: torch.dtype, ndims: tuple[int, ...]):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() not in ndims:
+        raise ValueError(f"{name} must have {' or '.join(map(str, ndims))} dims, got {t.dim()}")
+
+
+def _broadcast_strides(t: torch.Tensor, name: str, dims: tuple[int, ...], full: int):
+    """Strides of a per-head operand in its expanded form of `full` dims (missing dims: 0)."""
+    if t.shape[:1] != dims[:1]:
+        raise ValueError(f"{name} must start with dimension {dims[0]}, got {tuple(t.shape)}")
+    st = list(t.stride()) + [0] * (full - t.dim())
+    for i in range(1, t.dim()):
+        if t.shape[i] != dims[i]:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected prefix of {dims}")
+    return st
+
+
+def describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out):
+    """Build ``(ssu_shape_t, ssu_strides_t)`` for a set of tensors (no data is touched)."""
+    _expect(state_pool, "state_pool", torch.float32, (4,))
+    if state_batch_indices.dtype not in (torch.int32, torch.int64) or \
+            state_batch_indices.dim() != 1:
+        raise TypeError("state_batch_indices must be a 1-D int32 or int64 tensor")
+    _expect(x, "x", torch.bfloat16, (3,))
+    _expect(out, "out", torch.bfloat16, (3,))
+    _expect(dt, "dt", torch.bfloat16, (2, 3))
+    _expect(dt_bias, "dt_bias", torch.float32, (1, 2))
+    _expect(D, "D", torch.float32, (1, 2))
+    _expect(A, "A", torch.float32, (1, 3))
+    _expect(B, "B", torch.bfloat16, (3,))
+    _expect(C, "C", torch.bfloat16, (3,))
+    pool, H, P, N = state_pool.shape
+    bs = x.shape[0]
+    G = B.shape[1]
+    if tuple(x.shape) != (bs, H, P) or tuple(out.shape) != (bs, H, P):
+        raise ValueError(f"x and out must be [bs, H, P] = {(bs, H, P)}")
+    if tuple(B.shape) != (bs, G, N) or tuple(C.shape) != (bs, G, N):
+        raise ValueError(f"B and C must be [bs, G, N] = {(bs, G, N)}")
+    if state_batch_indices.shape[0] != bs:
+        raise ValueError("state_batch_indices must have one entry per request")
+    if tuple(dt.shape[:2]) != (bs, H) or (dt.dim() == 3 and dt.shape[2] != P):
+        raise ValueError("dt must be [bs, H] or [bs, H, P]")
+    shape = ssu_shape_t(bs, H, P, N, G, pool,
+                        SSU_INDEX_I64 if state_batch_indices.dtype == torch.int64
+                        else SSU_INDEX_I32, 0)
+    st = ssu_strides_t()
+    st.state[:] = list(state_pool.stride())
+    st.x[:] = list(x.stride())
+    st.out[:] = list(out.stride())
+    st.dt[:] = list(dt.stride()) + [0] * (3 - dt.dim())
+    st.B[:] = list(B.stride())
+    st.C[:] = list(C.stride())
+    st.dt_bias[:] = _broadcast_strides(dt_bias, "dt_bias", (H, P), 2)
+    st.D[:] = _broadcast_strides(D, "D", (H, P), 2)
+    st.A[:] = _broadcast_strides(A, "A", (H, P, N), 3)
+    st.idx = state_batch_indices.stride(0)
+    return shape, st
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---- the C entry points --------------------------------------------------------------------
+
+def ssu_abi_version() -> int:
+    return int(lib().ssu_abi_version())
+
+
+def ssu_create(device: int = 0) -> int:
+    """Create a handle on ``device``; returns it as an integer."""
+    h = _vp()
+    _check(lib().ssu_create(ctypes.byref(h), int(device)), "ssu_create")
+    return h.value
+
+
+def ssu_destroy(handle: int) -> None:
+    _check(lib().ssu_destroy(handle), "ssu_destroy")
+
+
+def ssu_validate(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out,
+                 shape: ssu_shape_t | None = None, strides: ssu_strides_t | None = None) -> int:
+    """Host-side validation only; returns the status code (0 = valid).
+
+    With tensors, the shape and strides are derived from them.  With integer pointers (no
+    memory is touched), ``shape`` and ``strides`` must be given.
+    """
+    if shape is None or strides is None:
+        shape, strides = describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
+                                  out)
+    ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)]
+    return int(lib().ssu_validate(*ptrs, ctypes.byref(shape), ctypes.byref(strides)))
+
+
+def ssu_update(handle: int, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out,
+               stream=None) -> None:
+    """Enqueue one decode step on ``stream`` (default: torch's current stream)."""
+    shape, strides = describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)
+    ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)]
+    _check(lib().ssu_update(handle, *ptrs, ctypes.byref(shape), ctypes.byref(strides),
+                            _stream_ptr(stream)), "ssu_update")
+
+
+def ssu_update_raw(handle: int, ptrs, shape: ssu_shape_t, strides: ssu_strides_t,
+                   stream: int | None) -> int:
+    """ssu_update with precomputed pointers/structs (for tight timing loops); returns status."""
+    return int(lib().ssu_update(handle, *ptrs, ctypes.byref(shape), ctypes.byref(strides),
+                                stream))
+
+
+def ssu_get_error(handle: int, stream=None) -> tuple[int, int]:
+    """Synchronise, then read and clear the skipped-request counters: (skipped, first_bad)."""
+    skipped = ctypes.c_uint32()
+    first = ctypes.c_int64()
+    st = lib().ssu_get_error(handle, _stream_ptr(stream), ctypes.byref(skipped),
+                             ctypes.byref(first))
+    if st not in (SSU_OK, SSU_ERR_INDEX_OOB):
+        _check(st, "ssu_get_error")
+    return int(skipped.value), int(first.value)
+
+
+def ssu_set_launch(handle: int, mode: int = SSU_MODE_AUTO, rows_per_warp: int = 0,
+                   warps_per_cta: int = 0, stages: int = 0) -> None:
+    """Force a launch shape (mode AUTO restores the built-in table)."""
+    cfg = ssu_launch_t(mode, rows_per_warp, warps_per_cta, stages)
+    _check(lib().ssu_set_launch(handle, ctypes.byref(cfg)), "ssu_set_launch")
+
+
+def ssu_get_launch(handle: int, shape: ssu_shape_t) -> tuple[int, int, int, int]:
+    cfg = ssu_launch_t()
+    _check(lib().ssu_get_launch(handle, ctypes.byref(shape), ctypes.byref(cfg)),
+           "ssu_get_launch")
+    return cfg.mode, cfg.rows_per_warp, cfg.warps_per_cta, cfg.stages
+
+
+class SelectiveStateUpdate:
+    """Owns one handle; ``__call__`` is ``ssu_update`` on it."""
+
+    def __init__(self, device: int | None = None):
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = int(device)
+        self.handle = ssu_create(self.device)
+
+    def __call__(self, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out,
+                 stream=None):
+        ssu_update(self.handle, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
+                   out, stream)
+        return out
+
+    def get_error(self, stream=None):
+        return ssu_get_error(self.handle, stream)
+
+    def set_launch(self, *args, **kw):
+        ssu_set_launch(self.handle, *args, **kw)
+
+    def close(self):
+        if self.handle:
+            ssu_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

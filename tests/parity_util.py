@@ -1,0 +1,109 @@
+"""Helpers shared by the GPU parity tests: moving problems to the device, running the oracle
+on sampled requests, and the tolerance rules.
+
+Tolerances (written here once, used by every parity test):
+
+* updated state: ``|S_gpu - S_ref| <= 1e-5 * (1 + |S_ref|)`` per element;
+* readout ``y`` (bf16): within 2 bf16 ulp of the oracle's correctly rounded value, or, where
+  ``y`` is small against the terms it sums (cancellation), within
+  ``2 * ulp_bf16(y_ref) + gamma * sum_n |S'_n C_n| + |D x| * 2^-23`` with
+  ``gamma = (N + 4) * 2^-24``, the classical forward error bound of an fp32 dot product of
+  length N plus the skip term;
+* indexing: bit-exact (untouched slots bit-identical, touched slots compared as above).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+STATE_RTOL = 1e-5
+Y_ULPS = 2
+
+
+def bf16_tensor(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_device(pr, dev="cuda", idx_dtype=torch.int32):
+    """Contiguous device tensors for a workloads.Problem."""
+    return dict(
+        state_pool=torch.from_numpy(pr.pool).to(dev),
+        state_batch_indices=torch.from_numpy(pr.idx).to(dev).to(idx_dtype),
+        x=bf16_tensor(pr.x, dev), dt=bf16_tensor(pr.dt, dev),
+        dt_bias=torch.from_numpy(pr.dt_bias).to(dev), A=torch.from_numpy(pr.A).to(dev),
+        B=bf16_tensor(pr.B, dev), C=bf16_tensor(pr.C, dev), D=torch.from_numpy(pr.D).to(dev),
+        out=torch.zeros(pr.x.shape, dtype=torch.bfloat16, device=dev))
+
+
+def ordered_bf16(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def ulp_bf16(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -126)
+    return np.where(a > 0, np.exp2(e - 7), 2.0 ** -133)
+
+
+def check_state(got: np.ndarray, ref: np.ndarray, what: str = "state") -> float:
+    got = got.astype(np.float64)
+    err = np.abs(got - ref) / (1.0 + np.abs(ref))
+    worst = float(err.max()) if err.size else 0.0
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    assert worst <= STATE_RTOL, f"{what}: max |err|/(1+|ref|) = {worst:.3e} > {STATE_RTOL}"
+    return worst
+
+
+def check_y(got_bits: np.ndarray, y_ref: np.ndarray, new_state_ref: np.ndarray,
+            C_ref: np.ndarray, Dx_ref: np.ndarray, N: int, what: str = "y") -> dict:
+    """got_bits [..., P] bf16 patterns; y_ref [..., P] float64; new_state_ref [..., P, N];
+    C_ref [..., N] broadcastable against new_state_ref's leading dims; Dx_ref like y_ref."""
+    ref_bits = oracle.bf16_rne(y_ref)
+    dist = np.abs(ordered_bf16(got_bits) - ordered_bf16(ref_bits))
+    gamma = (N + 4) * 2.0 ** -24
+    mag = np.abs(new_state_ref * C_ref[..., None, :]).sum(axis=-1)
+    got = oracle.bf16_to_f64(got_bits)
+    bound = Y_ULPS * ulp_bf16(y_ref) + gamma * mag + np.abs(Dx_ref) * 2.0 ** -23
+    ok_ulp = dist <= Y_ULPS
+    ok_abs = np.abs(got - y_ref) <= bound
+    bad = ~(ok_ulp | ok_abs)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} readouts out of tolerance; worst ulp "
+                           f"distance {int(dist.max())}")
+    return {"max_ulp": int(dist.max()) if dist.size else 0,
+            "abs_rule_used": int((~ok_ulp).sum())}
+
+
+def oracle_on_requests(pool_host: np.ndarray, idx: np.ndarray, rows: np.ndarray, x, dt,
+                       dt_bias, A, B, C, D, ngroups: int = 1):
+    """Run the oracle on requests ``rows`` only.
+
+    The sampled requests' slots are gathered from the (pre-step) host pool into a small pool
+    whose slot j holds request rows[j]'s state, so the oracle's own slot lookup still runs.
+    Returns (new_states [k,H,P,N] float64, y [k,H,P] float64).
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    slots = idx[rows]
+    sub = pool_host[slots].astype(np.float64)
+    local = np.arange(len(rows), dtype=np.int64)
+    y, skipped = oracle.ssu_step_inplace(sub, local, x[rows], dt[rows], dt_bias, A, B[rows],
+                                         C[rows], D, ngroups)
+    assert skipped == 0
+    return sub, y
+
+
+def expected_terms(x_bits, D, C_bits, ngroups: int, H: int):
+    """(C per head [k,H,N] float64, D*x [k,H,P] float64) for the readout tolerance."""
+    Cf = oracle.bf16_to_f64(C_bits)                 # [k, G, N]
+    g = np.arange(H) // (H // ngroups)
+    Ch = Cf[:, g, :]                                 # [k, H, N]
+    Dx = np.asarray(D, dtype=np.float64)[None, :, None] * oracle.bf16_to_f64(x_bits)
+    return Ch, Dx
