@@ -525,6 +525,47 @@ def _smi_index(local: int) -> int:
     return local
 
 
+SWEEP_SHAPES = ([(1, r, w, 0) for r in (1, 2, 4, 8, 16) for w in (1, 2, 4, 8)] +
+                [(2, r, w, st) for r, w in ((4, 4), (8, 2), (8, 4), (16, 2), (16, 4), (8, 8),
+                                            (4, 8), (2, 8))
+                 for st in (2, 3, 4, 6) if st * r * w * 512 <= 200 * 1024])
+
+
+def run_sweep(args) -> None:
+    """Launch-shape sweep: every (rows per warp, warps per CTA) at batch 8, 128 and 512 on the
+    cold-L2 rotation workloads; one JSON line per point, then the fastest shape per batch."""
+    import torch
+
+    import selective_state_update_02_gb300 as ssu
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = ssu.ssu_create(0)
+    best = {}
+    for bs in args.sweep_batches:
+        w = Workload(bs, NHEADS, dev, seed=200 + bs, l2_bytes=l2)
+        n = max(1000, int(args.sweep_us_budget / (0.16 * bs + 2.0)))
+        for mode, rpw, wpc, stages in SWEEP_SHAPES:
+            ssu.ssu_set_launch(handle, mode, rpw, wpc, stages)
+            ms, _, _ = time_calls(w, handle, n, 5)
+            us = ms * 1000.0 / n
+            rec = {"batch": bs, "mode": "vec" if mode == 1 else "bulk", "rows_per_warp": rpw,
+                   "warps_per_cta": wpc, "stages": stages, "us_per_call": round(us, 3),
+                   "tbps": round(bytes_per_call(bs) / (us * 1e-6) / 1e12, 3), "steps": n}
+            print(json.dumps(rec), flush=True)
+            if bs not in best or us < best[bs]["us_per_call"]:
+                best[bs] = rec
+        ssu.ssu_set_launch(handle, ssu.SSU_MODE_AUTO)
+        ms, _, _ = time_calls(w, handle, n, 5)
+        us = ms * 1000.0 / n
+        launch = ssu.ssu_get_launch(handle, w.args[0][1])
+        print(json.dumps({"batch": bs, "mode": "table", "launch": launch,
+                          "us_per_call": round(us, 3)}), flush=True)
+        del w
+        torch.cuda.empty_cache()
+    print(json.dumps({"best": best}), flush=True)
+    ssu.ssu_destroy(handle)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -536,10 +577,16 @@ def main() -> None:
     ap.add_argument("--skip-extra", action="store_true", help="skip the batch 8/512 lines")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="launch-shape sweep instead")
+    ap.add_argument("--sweep-batches", type=int, nargs="+", default=[8, 128, 512])
+    ap.add_argument("--sweep-us-budget", type=float, default=60000.0,
+                    help="approximate GPU time per sweep point, microseconds")
     args = ap.parse_args()
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -55,7 +55,9 @@ typedef enum {
     SSU_ERR_UNSUPPORTED = 2, /* a size or stride form this build does not implement */
     SSU_ERR_MISALIGNED = 3,  /* state_pool base or a state stride not a multiple of 16 bytes */
     SSU_ERR_CUDA = 4,        /* a CUDA runtime call failed; ssu_last_error() names it */
-    SSU_ERR_INDEX_OOB = 5    /* ssu_get_error: at least one request was skipped */
+    SSU_ERR_INDEX_OOB = 5,   /* ssu_get_error: at least one request was skipped */
+    SSU_ERR_TIMEOUT = 6      /* ssu_get_error: a BULK pipeline wait gave up after 1 s; the
+                                call's results are incomplete (never expected; a defect) */
 } ssu_status_t;
 
 typedef enum { SSU_INDEX_I32 = 0, SSU_INDEX_I64 = 1 } ssu_index_dtype_t;
@@ -94,15 +96,20 @@ typedef struct {
 /* Launch shapes of the streaming kernel. */
 typedef enum {
     SSU_MODE_AUTO = 0,   /* use the built-in table (the default) */
-    SSU_MODE_VEC = 1,    /* 16-byte vector loads and stores straight from registers */
-    SSU_MODE_BULK = 2    /* bulk asynchronous copies through shared memory */
+    SSU_MODE_VEC = 1,    /* one CTA per tile; 16-byte vector loads/stores through registers */
+    SSU_MODE_BULK = 2    /* persistent CTAs; bulk asynchronous copies (TMA engine) of whole
+                            tiles through a ring of shared-memory stages.  Needs contiguous
+                            state rows (state row stride == dstate); the table falls back to
+                            VEC otherwise, a forced BULK shape returns SSU_ERR_UNSUPPORTED */
 } ssu_mode_t;
 
+/* A tile is rows_per_warp * warps_per_cta consecutive state rows of one (request, head). */
 typedef struct {
     int32_t mode;          /* ssu_mode_t */
-    int32_t rows_per_warp; /* VEC: state rows (of N floats) one warp streams: 1,2,4,8,16 */
-    int32_t warps_per_cta; /* VEC: 1..16; BULK: compute warps per CTA, 1..16 */
-    int32_t stages;        /* BULK: shared-memory pipeline depth, 2..8; VEC: ignored */
+    int32_t rows_per_warp; /* rows each warp updates per tile: VEC 1,2,4,8,16; BULK 2,4,8,16 */
+    int32_t warps_per_cta; /* VEC: 1..16 warps; BULK: 1..8 compute warps (plus one producer) */
+    int32_t stages;        /* BULK: shared-memory ring depth, 2..8 (stages x tile <= the
+                              device's shared memory per CTA); VEC: ignored */
 } ssu_launch_t;
 
 /* ABI version this library was built with (SSU_ABI_VERSION). */
@@ -148,10 +155,11 @@ ssu_status_t ssu_update(ssu_handle_t handle, float *state_pool, const void *stat
                         ssu_stream_t stream);
 
 /*
- * Synchronise `stream`, then read and clear the handle's skipped-request counters.
+ * Synchronise `stream`, then read and clear the handle's device counters.
  * *skipped receives the number of requests skipped since the last read (may be NULL);
  * *first_bad receives the smallest skipped request index b, or -1 (may be NULL).
- * Returns SSU_ERR_INDEX_OOB when *skipped > 0, SSU_OK otherwise.
+ * Returns SSU_ERR_TIMEOUT if a BULK pipeline wait gave up, else SSU_ERR_INDEX_OOB when
+ * *skipped > 0, SSU_OK otherwise.
  */
 ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *skipped,
                            int64_t *first_bad);

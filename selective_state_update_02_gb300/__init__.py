@@ -29,6 +29,7 @@ SSU_ERR_UNSUPPORTED = 2
 SSU_ERR_MISALIGNED = 3
 SSU_ERR_CUDA = 4
 SSU_ERR_INDEX_OOB = 5
+SSU_ERR_TIMEOUT = 6
 
 SSU_INDEX_I32 = 0
 SSU_INDEX_I64 = 1

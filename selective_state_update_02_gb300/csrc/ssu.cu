@@ -5,23 +5,37 @@
 // standard Mamba2 decode step).  The step is bound by HBM traffic: per (request, head) unit it
 // reads and writes a 64 x 128 fp32 state (32 KiB each way) and touches ~2.5 KiB of inputs.
 // There is no dense contraction here, so no tensor cores: the design goal is to keep enough
-// bytes in flight to saturate HBM3e, with every access a full 16-byte vector per lane.
+// bytes in flight to saturate HBM3e.
 //
-// Work decomposition ("VEC" mode).  A warp owns `RPW` consecutive state rows of one unit;
-// lane l owns columns 4l..4l+3 of each row, so each row is one fully coalesced 512-byte
-// access per warp and a warp keeps RPW x 512 bytes of loads in flight.  A CTA holds
-// `warps_per_cta` such warps over consecutive rows of the same unit.  B[n] and C[n] are read
-// straight into registers (each lane needs only its own 4 columns); x[p], dt, dt_bias, A, D
-// are warp-uniform broadcast loads.  Each row's readout sum over dstate is the lane's 4-term
-// chain followed by a xor-butterfly over the 32 lanes in the fixed mask order 16,8,4,2,1.
-// Because that order never depends on RPW or warps_per_cta, every launch shape produces
-// bit-identical state and output.
+// Element mapping shared by both kernels.  A state row is dstate = 128 fp32 = 512 bytes; lane
+// l of a warp owns columns 4l..4l+3 of a row, so one row is one fully used 512-byte access per
+// warp.  B[n] and C[n] are read straight into registers (each lane needs only its own 4
+// columns); x[p], dt, dt_bias, A and D are per-tile scalars.  Each element is updated as
+// fmaf(S, dA, (dtv * x[p]) * B[n]); each row's readout is the lane's 4-term chain followed by a
+// xor butterfly over the 32 lanes in the fixed mask order 16, 8, 4, 2, 1.  Nothing in that
+// order depends on the launch shape, so every shape of both kernels gives bit-identical state
+// and output.
+//
+// VEC kernel: one CTA per (request, head, slab of rows).  Each warp loads RPW rows as 16-byte
+// vectors into registers (all loads issued before any use), updates them, stores them back in
+// place and writes the readout.  Bytes in flight are bounded by registers and occupancy.
+//
+// BULK kernel: persistent CTAs (as many as fit on the SMs) stream tiles of `tile_rows` rows
+// through a ring of shared-memory stages.  Warp 0 is the producer: it reads the slot index of
+// each tile ahead of time and issues a bulk asynchronous copy (the TMA engine's 1-D
+// `cp.async.bulk`) of the tile's contiguous rows into a free stage, completion counted on the
+// stage's mbarrier.  The compute warps read their rows out of the stage into registers, hand
+// the stage back at once (the producer refills it while they work), update the rows and store
+// them in place with 16-byte vector stores, and write the readout.  Loads in flight are bounded
+// by shared memory (stages x tile), not by registers.  Every mbarrier wait is bounded in time;
+// a timeout raises an error counter and the CTA stops after its copies in flight have landed.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -30,8 +44,12 @@
 
 namespace {
 
-constexpr int kDstate = 128;  // dstate this build implements: 32 lanes x 4 columns
-constexpr int kMaxWarpsPerCta = 16;
+constexpr int kDstate = 128;             // dstate this build implements: 32 lanes x 4 columns
+constexpr int kRowBytes = kDstate * 4;   // one fp32 state row
+constexpr int kMaxWarpsPerCta = 16;      // VEC
+constexpr int kMaxBulkWarps = 8;         // BULK compute warps (plus one producer warp)
+constexpr int kMaxStages = 8;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per mbarrier wait
 
 // Everything one launch needs, passed by value in the kernel parameter space.
 struct SsuParams {
@@ -51,9 +69,15 @@ struct SsuParams {
     long long bias_h, D_h, A_h, idx_s;
     long long pool_size;
     int nheads, headdim, heads_per_group;
-    int slabs;         // CTAs per unit
-    int rows_per_cta;  // RPW * warps_per_cta
-    unsigned *err;     // [0] skipped requests, [1] smallest skipped request index
+    int slabs;         // tiles per (request, head) unit
+    int rows_per_cta;  // rows per tile
+    unsigned *err;     // [0] skipped requests, [1] smallest skipped request, [2] timeouts
+};
+
+// BULK launch geometry.
+struct BulkShape {
+    long long tiles;  // batch * nheads * slabs
+    int stages;
 };
 
 __device__ __forceinline__ float softplus_f32(float z) {
@@ -61,13 +85,59 @@ __device__ __forceinline__ float softplus_f32(float z) {
     return z > 20.0f ? z : log1pf(expf(z));
 }
 
-__device__ __forceinline__ float butterfly_sum(float v) {
-    v += __shfl_xor_sync(0xffffffffu, v, 16);
-    v += __shfl_xor_sync(0xffffffffu, v, 8);
-    v += __shfl_xor_sync(0xffffffffu, v, 4);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    return v;
+// The update of one lane's 4 columns of one row; returns the lane's part of the readout.
+__device__ __forceinline__ float update_cols(float4 &w, float dA, float k, const float (&bb)[4],
+                                             const float (&cc)[4]) {
+    w.x = fmaf(w.x, dA, k * bb[0]);
+    w.y = fmaf(w.y, dA, k * bb[1]);
+    w.z = fmaf(w.z, dA, k * bb[2]);
+    w.w = fmaf(w.w, dA, k * bb[3]);
+    float part = w.x * cc[0];
+    part = fmaf(w.y, cc[1], part);
+    part = fmaf(w.z, cc[2], part);
+    part = fmaf(w.w, cc[3], part);
+    return part;
+}
+
+// Sums R per-lane parts (one per row) over the 32 lanes.  The pairs are always formed by xor
+// masks 16, 8, 4, 2, 1 in that order (the tree of a plain butterfly), but while a lane holds
+// more than one row it hands half of its rows to its partner at each step ("reduce-scatter"),
+// which needs R - 1 + (5 - log2 R) shuffles instead of 5 R.  Each sum is the same IEEE value the
+// plain butterfly gives (a + b == b + a exactly), whatever R is.  Afterwards lane l holds the
+// total of row row_of_lane<R>(l).
+template <int R>
+__device__ __forceinline__ float reduce_rows(float (&v)[R], int lane) {
+    static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
+#pragma unroll
+    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const float give = upper ? v[j] : v[j + n / 2];
+            const float keep = upper ? v[j + n / 2] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int m = 16 / R; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+    return t;
+}
+
+// The row whose total lane l holds after reduce_rows<R>.
+template <int R>
+__device__ __forceinline__ int row_of_lane(int lane) {
+    int row = 0;
+#pragma unroll
+    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1)
+        if (lane & m) row += n / 2;
+    return row;
+}
+
+// Lanes that write a readout: one per group of lanes holding the same row.
+template <int R>
+__device__ __forceinline__ bool writes_row(int lane) {
+    return (lane & (32 / R - 1)) == 0;
 }
 
 template <bool kIdx64>
@@ -75,6 +145,14 @@ __device__ __forceinline__ long long load_slot(const SsuParams &p, long long b) 
     if (kIdx64) return __ldg(static_cast<const long long *>(p.idx) + b * p.idx_s);
     return static_cast<long long>(__ldg(static_cast<const int *>(p.idx) + b * p.idx_s));
 }
+
+__device__ __forceinline__ void record_skip(const SsuParams &p, long long b) {
+    atomicAdd(&p.err[0], 1u);
+    atomicMin(&p.err[1], static_cast<unsigned>(b));
+}
+
+// ---------------------------------------------------------------------------------------
+// VEC kernel
 
 template <int RPW, bool kIdx64>
 __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
@@ -89,10 +167,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
 
     const long long s = load_slot<kIdx64>(p, b);
     if (s < 0 || s >= p.pool_size) {
-        if (h == 0 && slab == 0 && threadIdx.x == 0) {
-            atomicAdd(&p.err[0], 1u);
-            atomicMin(&p.err[1], static_cast<unsigned>(b));
-        }
+        if (h == 0 && slab == 0 && threadIdx.x == 0) record_skip(p, b);
         return;
     }
 
@@ -117,35 +192,303 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     const int g = h / p.heads_per_group;
     const __nv_bfloat16 *Bp = p.B + b * p.B_b + g * p.B_g + lane * 4;
     const __nv_bfloat16 *Cp = p.C + b * p.C_b + g * p.C_g + lane * 4;
-    const float b0 = __bfloat162float(Bp[0]), b1 = __bfloat162float(Bp[1]);
-    const float b2 = __bfloat162float(Bp[2]), b3 = __bfloat162float(Bp[3]);
-    const float c0 = __bfloat162float(Cp[0]), c1 = __bfloat162float(Cp[1]);
-    const float c2 = __bfloat162float(Cp[2]), c3 = __bfloat162float(Cp[3]);
+    float bb[4], cc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        bb[j] = __bfloat162float(Bp[j]);
+        cc[j] = __bfloat162float(Cp[j]);
+    }
     const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
 
-    float mine = 0.f;  // lane r keeps the readout of row row0 + r
+    float part[RPW];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
-        if (row0 + r < p.headdim) {
-            const float xr = __bfloat162float(xp[r]);
-            const float k = dtv * xr;
-            float4 w = v[r];
-            w.x = fmaf(w.x, dA, k * b0);
-            w.y = fmaf(w.y, dA, k * b1);
-            w.z = fmaf(w.z, dA, k * b2);
-            w.w = fmaf(w.w, dA, k * b3);
-            __stcs(reinterpret_cast<float4 *>(srow + r * p.st_row), w);
-            float part = w.x * c0;
-            part = fmaf(w.y, c1, part);
-            part = fmaf(w.z, c2, part);
-            part = fmaf(w.w, c3, part);
-            const float y = fmaf(Dh, xr, butterfly_sum(part));
-            if (lane == r) mine = y;
+        const bool live = row0 + r < p.headdim;
+        const float xr = live ? __bfloat162float(xp[r]) : 0.f;
+        part[r] = update_cols(v[r], dA, dtv * xr, bb, cc);
+        if (live) __stcs(reinterpret_cast<float4 *>(srow + r * p.st_row), v[r]);
+    }
+    const float total = reduce_rows<RPW>(part, lane);
+    const int rl = row_of_lane<RPW>(lane);
+    if (writes_row<RPW>(lane) && row0 + rl < p.headdim) {
+        const float xr = __bfloat162float(xp[rl]);
+        p.out[b * p.out_b + h * p.out_h + row0 + rl] = __float2bfloat16_rn(fmaf(Dh, xr, total));
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// BULK kernel: PTX helpers (mbarrier, bulk asynchronous copies, proxy fence)
+
+__device__ __forceinline__ unsigned smem_u32(const void *ptr) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `parity` to complete; false after kWaitLimitNs without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 32; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, unsigned bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Shared-memory layout of the BULK kernel: barriers and per-stage slots, then the stages.
+struct BulkSmem {
+    uint64_t *full;   // [stages] producer -> compute: stage loaded (or its tile skipped)
+    uint64_t *freed;  // [stages] compute -> producer: every compute warp has read the stage
+    long long *slot;  // [stages] slot of the tile in the stage, -1 when skipped
+    float *buf;       // [stages][tile_rows][128]
+};
+
+__host__ __device__ constexpr unsigned bulk_header_bytes(int stages) {
+    return ((static_cast<unsigned>(stages) * 24u + 127u) / 128u) * 128u;
+}
+
+__device__ __forceinline__ BulkSmem bulk_smem(unsigned char *base, int stages) {
+    BulkSmem s;
+    s.full = reinterpret_cast<uint64_t *>(base);
+    s.freed = s.full + stages;
+    s.slot = reinterpret_cast<long long *>(s.freed + stages);
+    s.buf = reinterpret_cast<float *>(base + bulk_header_bytes(stages));
+    return s;
+}
+
+// Coordinates of global tile t.
+struct TileCoord {
+    long long b;
+    int h, row0, rows;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const SsuParams &p, long long t) {
+    TileCoord c;  // t < 2^31 (checked on the host), so 32-bit division suffices
+    const unsigned tt = static_cast<unsigned>(t);
+    const unsigned unit = tt / static_cast<unsigned>(p.slabs);
+    const int slab = static_cast<int>(tt - unit * static_cast<unsigned>(p.slabs));
+    c.h = static_cast<int>(unit % static_cast<unsigned>(p.nheads));
+    c.b = static_cast<long long>(unit / static_cast<unsigned>(p.nheads));
+    c.row0 = slab * p.rows_per_cta;
+    c.rows = min(p.rows_per_cta, p.headdim - c.row0);
+    return c;
+}
+
+// Per-tile inputs of one compute warp, loaded one tile ahead of their use.
+struct TileInputs {
+    float dt, bias, A, D;
+    float bb[4], cc[4];
+    float x;  // lane r < RPW: x of this warp's row r of the tile
+};
+
+template <int RPW>
+__device__ __forceinline__ TileInputs load_tile_inputs(const SsuParams &p, const TileCoord &c,
+                                                       int cw, int lane) {
+    TileInputs in;
+    const long long b = c.b;
+    const int h = c.h;
+    in.dt = __bfloat162float(p.dt[b * p.dt_b + h * p.dt_h]);
+    in.bias = p.dt_bias[h * p.bias_h];
+    in.A = p.A[h * p.A_h];
+    in.D = p.D[h * p.D_h];
+    const int g = h / p.heads_per_group;
+    const __nv_bfloat16 *Bp = p.B + b * p.B_b + g * p.B_g + lane * 4;
+    const __nv_bfloat16 *Cp = p.C + b * p.C_b + g * p.C_g + lane * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        in.bb[j] = __bfloat162float(Bp[j]);
+        in.cc[j] = __bfloat162float(Cp[j]);
+    }
+    const int row = cw * RPW + lane;
+    in.x = (lane < RPW && row < c.rows)
+               ? __bfloat162float(p.x[b * p.x_b + h * p.x_h + c.row0 + row])
+               : 0.f;
+    return in;
+}
+
+// Producer warp 0 issues the bulk loads; compute warps 1..W update rows and store them from
+// registers.  A stage is handed back to the producer as soon as every compute warp has read
+// its rows out of it, so the producer refills it while the update and the stores proceed.
+template <int RPW, bool kIdx64>
+__global__ void __launch_bounds__(32 * (1 + kMaxBulkWarps))
+    ssu_bulk_kernel(const __grid_constant__ SsuParams p, const BulkShape q) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int stages = q.stages;
+    const BulkSmem sm = bulk_smem(smem_raw, stages);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int compute_warps = static_cast<int>(blockDim.x >> 5) - 1;
+    const long long G = gridDim.x;
+    const long long cta = blockIdx.x;
+    const long long n_my = (q.tiles - cta + G - 1) / G;  // tiles cta, cta + G, ...
+    constexpr int kRowFloats = kDstate;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.freed[s], static_cast<unsigned>(32 * compute_warps));
+        }
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------- producer warp ----------------
+        // Slots of this CTA's tiles in windows of 32 (lane l holds tile win + l); the next
+        // window is loaded one window ahead.
+        auto slot_of_tile = [&](long long i) -> long long {
+            if (i >= n_my) return -1;
+            const TileCoord c = tile_coord(p, cta + i * G);
+            return load_slot<kIdx64>(p, c.b);
+        };
+        long long win = 0;
+        long long win_cur = slot_of_tile(lane);
+        long long win_next = slot_of_tile(32 + lane);
+        auto issue_load = [&](long long j) {
+            if (j >= win + 32) {  // j advances by one per call
+                win += 32;
+                win_cur = win_next;
+                win_next = slot_of_tile(win + 32 + lane);
+            }
+            const long long s = __shfl_sync(0xffffffffu, win_cur, static_cast<int>(j - win));
+            const int st = static_cast<int>(j % stages);
+            const TileCoord c = tile_coord(p, cta + j * G);
+            const bool valid = s >= 0 && s < p.pool_size;
+            if (lane == 0) {
+                sm.slot[st] = valid ? s : -1;
+                if (valid) {
+                    const unsigned bytes = static_cast<unsigned>(c.rows) * kRowBytes;
+                    mbar_arrive_expect_tx(&sm.full[st], bytes);
+                    bulk_load(sm.buf + static_cast<size_t>(st) * p.rows_per_cta * kRowFloats,
+                              p.state + s * p.st_pool + c.h * p.st_head + c.row0 * p.st_row,
+                              bytes, &sm.full[st]);
+                } else {
+                    if (c.h == 0 && c.row0 == 0) record_skip(p, c.b);
+                    mbar_arrive(&sm.full[st]);
+                }
+            }
+            __syncwarp();
+        };
+        const long long first = n_my < stages ? n_my : stages;
+        for (long long j = 0; j < first; ++j) issue_load(j);
+        long long issued = first;
+        bool failed = false;
+        for (long long i = 0; i + stages < n_my; ++i) {
+            const int st = static_cast<int>(i % stages);
+            const bool ok = mbar_wait(&sm.freed[st], static_cast<unsigned>((i / stages) & 1));
+            if (!__all_sync(0xffffffffu, ok)) {
+                failed = true;
+                break;
+            }
+            issue_load(i + stages);
+            issued = i + stages + 1;
+        }
+        if (failed && lane == 0) {
+            atomicAdd(&p.err[2], 1u);
+            // Loads in flight must land before the CTA's shared memory is released; each of
+            // these waits is bounded too.
+            for (long long j = issued > stages ? issued - stages : 0; j < issued; ++j)
+                mbar_wait(&sm.full[j % stages], static_cast<unsigned>((j / stages) & 1));
+        }
+    } else {
+        // ---------------- compute warps ----------------
+        const int cw = warp - 1;
+        const int r0 = cw * RPW;  // this warp's first row within a tile
+        TileInputs cur{};
+        if (n_my > 0) cur = load_tile_inputs<RPW>(p, tile_coord(p, cta), cw, lane);
+        for (long long i = 0; i < n_my; ++i) {
+            const int st = static_cast<int>(i % stages);
+            const TileCoord c = tile_coord(p, cta + i * G);
+            TileInputs nxt = cur;
+            if (i + 1 < n_my)
+                nxt = load_tile_inputs<RPW>(p, tile_coord(p, cta + (i + 1) * G), cw, lane);
+            const bool ok = mbar_wait(&sm.full[st], static_cast<unsigned>((i / stages) & 1));
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) atomicAdd(&p.err[2], 1u);
+                break;
+            }
+            const long long s = sm.slot[st];
+            // Read this warp's rows out of the stage, then hand the stage back.
+            const float *stage = sm.buf + static_cast<size_t>(st) * p.rows_per_cta * kRowFloats;
+            float4 v[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                v[r] = (s >= 0 && r0 + r < c.rows)
+                           ? reinterpret_cast<const float4 *>(stage + (r0 + r) * kRowFloats)[lane]
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            mbar_arrive(&sm.freed[st]);  // every lane: its reads precede the refill
+            if (s >= 0) {
+                const float dtv = softplus_f32(cur.dt + cur.bias);
+                const float dA = expf(dtv * cur.A);
+                float *srow = p.state + s * p.st_pool + c.h * p.st_head +
+                              (c.row0 + r0) * p.st_row + lane * 4;
+                float part[RPW];
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    const float xr = __shfl_sync(0xffffffffu, cur.x, r);
+                    part[r] = update_cols(v[r], dA, dtv * xr, cur.bb, cur.cc);
+                    if (r0 + r < c.rows)
+                        __stcs(reinterpret_cast<float4 *>(srow + r * p.st_row), v[r]);
+                }
+                const float total = reduce_rows<RPW>(part, lane);
+                const int rl = row_of_lane<RPW>(lane);
+                const float xr = __shfl_sync(0xffffffffu, cur.x, rl);
+                if (writes_row<RPW>(lane) && r0 + rl < c.rows)
+                    p.out[c.b * p.out_b + c.h * p.out_h + c.row0 + r0 + rl] =
+                        __float2bfloat16_rn(fmaf(cur.D, xr, total));
+            }
+            cur = nxt;
         }
     }
-    if (lane < RPW && row0 + lane < p.headdim)
-        p.out[b * p.out_b + h * p.out_h + row0 + lane] = __float2bfloat16_rn(mine);
 }
+
+// ---------------------------------------------------------------------------------------
+// Launchers
 
 template <bool kIdx64>
 cudaError_t launch_vec(const SsuParams &p, int rpw, int wpc, unsigned grid, cudaStream_t st) {
@@ -159,6 +502,22 @@ cudaError_t launch_vec(const SsuParams &p, int rpw, int wpc, unsigned grid, cuda
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+using BulkKernel = void (*)(SsuParams, BulkShape);
+
+BulkKernel bulk_kernel(int rpw, bool idx64) {
+    switch (rpw) {
+        case 2: return idx64 ? ssu_bulk_kernel<2, true> : ssu_bulk_kernel<2, false>;
+        case 4: return idx64 ? ssu_bulk_kernel<4, true> : ssu_bulk_kernel<4, false>;
+        case 8: return idx64 ? ssu_bulk_kernel<8, true> : ssu_bulk_kernel<8, false>;
+        case 16: return idx64 ? ssu_bulk_kernel<16, true> : ssu_bulk_kernel<16, false>;
+        default: return nullptr;
+    }
+}
+
+unsigned bulk_smem_bytes(int stages, int tile_rows) {
+    return bulk_header_bytes(stages) + static_cast<unsigned>(stages) * tile_rows * kRowBytes;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -223,6 +582,7 @@ ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint1
                     (long long)s.dstate);
     if (s.headdim > (1 << 20) || s.nheads > (1 << 20))
         return fail(SSU_ERR_UNSUPPORTED, "headdim and nheads are limited to 2^20");
+    if (s.batch == 0) return ok();  // nothing is read or written: strides are irrelevant
 
     const int64_t *all[] = {st->state, st->x, st->out, st->dt, st->B, st->C,
                             st->dt_bias, st->D, st->A};
@@ -246,7 +606,6 @@ ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint1
             return fail(SSU_ERR_MISALIGNED, "state stride %d (%lld) is not a multiple of 4 floats",
                         j, (long long)st->state[j]);
 
-    if (s.batch == 0) return ok();
     if (!state_pool || !idx || !x || !dt || !dt_bias || !A || !B || !C || !D || !out)
         return fail(SSU_ERR_INVALID_ARG, "a data pointer is NULL");
     if (!aligned(state_pool, 16))
@@ -262,22 +621,19 @@ ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint1
     return ok();
 }
 
-bool launch_shape_ok(const ssu_launch_t &l) {
-    if (l.mode != SSU_MODE_VEC) return false;
-    const int r = l.rows_per_warp;
-    if (r != 1 && r != 2 && r != 4 && r != 8 && r != 16) return false;
-    return l.warps_per_cta >= 1 && l.warps_per_cta <= kMaxWarpsPerCta;
+bool is_pow2_rows(int r, int lo, int hi) {
+    return r >= lo && r <= hi && (r & (r - 1)) == 0;
 }
 
-// Built-in launch-shape table.  8 rows per warp (32 floats, 128 bytes of loads in flight
-// per thread) with few warps per CTA; the CTA count then spreads small batches over all SMs.
-ssu_launch_t table_launch(const ssu_shape_t &s, int sm_count) {
-    ssu_launch_t l{SSU_MODE_VEC, 8, 1, 0};
-    const long long rows = s.batch * s.nheads * s.headdim;
-    const long long warps_needed = (rows + 7) / 8;
-    // Batches large enough to give every SM many warps use 2-warp CTAs.
-    if (warps_needed >= 16LL * sm_count) l.warps_per_cta = 2;
-    return l;
+// Checks a launch shape by itself (sizes the kernels accept).
+bool launch_shape_ok(const ssu_launch_t &l) {
+    if (l.mode == SSU_MODE_VEC)
+        return is_pow2_rows(l.rows_per_warp, 1, 16) && l.warps_per_cta >= 1 &&
+               l.warps_per_cta <= kMaxWarpsPerCta;
+    if (l.mode == SSU_MODE_BULK)
+        return is_pow2_rows(l.rows_per_warp, 2, 16) && l.warps_per_cta >= 1 &&
+               l.warps_per_cta <= kMaxBulkWarps && l.stages >= 2 && l.stages <= kMaxStages;
+    return false;
 }
 
 }  // namespace
@@ -285,10 +641,32 @@ ssu_launch_t table_launch(const ssu_shape_t &s, int sm_count) {
 struct ssu_handle_s {
     int device = 0;
     int sm_count = 0;
-    unsigned *err = nullptr;  // device: [0] skipped count, [1] smallest skipped request
+    int smem_optin = 0;       // max dynamic shared memory per CTA (bytes)
+    unsigned *err = nullptr;  // device: [0] skipped, [1] smallest skipped request, [2] timeouts
     bool has_override = false;
     ssu_launch_t override_launch{};
 };
+
+namespace {
+
+// Built-in launch-shape table (measured on GB300 with the cold-L2 rotation workloads).
+ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
+    ssu_launch_t l{SSU_MODE_VEC, 8, 1, 0};
+    const long long rows = s.batch * s.nheads * s.headdim;
+    const long long warps_needed = (rows + 7) / 8;
+    if (warps_needed >= 16LL * hd.sm_count) l.warps_per_cta = 2;
+    (void)st;
+    return l;
+}
+
+// Whether the BULK kernel can run this call (contiguous rows; shared memory fits).
+bool bulk_fits(const ssu_handle_s &hd, const ssu_launch_t &l, const ssu_strides_t *st) {
+    if (st->state[2] != kDstate) return false;
+    const int tile_rows = l.rows_per_warp * l.warps_per_cta;
+    return static_cast<int>(bulk_smem_bytes(l.stages, tile_rows)) <= hd.smem_optin;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -302,6 +680,7 @@ const char *ssu_status_string(ssu_status_t status) {
         case SSU_ERR_MISALIGNED: return "SSU_ERR_MISALIGNED";
         case SSU_ERR_CUDA: return "SSU_ERR_CUDA";
         case SSU_ERR_INDEX_OOB: return "SSU_ERR_INDEX_OOB";
+        case SSU_ERR_TIMEOUT: return "SSU_ERR_TIMEOUT";
     }
     return "SSU_ERR_UNKNOWN";
 }
@@ -321,6 +700,13 @@ ssu_status_t ssu_create(ssu_handle_t *out, int32_t device) {
     ssu_handle_s *h = new ssu_handle_s();
     h->device = device;
     e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                   device);
+    for (int rpw = 2; e == cudaSuccess && rpw <= 16; rpw *= 2)
+        for (int i64 = 0; e == cudaSuccess && i64 < 2; ++i64)
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(bulk_kernel(rpw, i64 != 0)),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin);
     if (e == cudaSuccess) e = cudaMalloc(&h->err, 4 * sizeof(unsigned));
     const unsigned init[4] = {0u, 0xffffffffu, 0u, 0u};
     if (e == cudaSuccess) e = cudaMemcpy(h->err, init, sizeof(init), cudaMemcpyHostToDevice);
@@ -357,7 +743,7 @@ ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
                             ssu_launch_t *launch) {
     if (!handle || !shape || !launch) return fail(SSU_ERR_INVALID_ARG, "NULL argument");
     *launch = handle->has_override ? handle->override_launch
-                                   : table_launch(*shape, handle->sm_count);
+                                   : table_launch(*handle, *shape, nullptr);
     return ok();
 }
 
@@ -368,8 +754,14 @@ ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch) {
         return ok();
     }
     if (!launch_shape_ok(*launch))
-        return fail(SSU_ERR_UNSUPPORTED, "launch shape mode=%d rows_per_warp=%d warps=%d",
-                    launch->mode, launch->rows_per_warp, launch->warps_per_cta);
+        return fail(SSU_ERR_UNSUPPORTED,
+                    "launch shape mode=%d rows_per_warp=%d warps=%d stages=%d", launch->mode,
+                    launch->rows_per_warp, launch->warps_per_cta, launch->stages);
+    if (launch->mode == SSU_MODE_BULK &&
+        static_cast<int>(bulk_smem_bytes(launch->stages,
+                                         launch->rows_per_warp * launch->warps_per_cta)) >
+            handle->smem_optin)
+        return fail(SSU_ERR_UNSUPPORTED, "BULK stages x tile exceed shared memory");
     handle->override_launch = *launch;
     handle->has_override = true;
     return ok();
@@ -385,12 +777,19 @@ ssu_status_t ssu_update(ssu_handle_t handle, float *state_pool, const void *stat
                                     D, out, shape, strides);
     if (st != SSU_OK || shape->batch == 0) return st;
     const ssu_shape_t &s = *shape;
-    const ssu_launch_t l = handle->has_override ? handle->override_launch
-                                                : table_launch(s, handle->sm_count);
-    const int rows_per_cta = l.rows_per_warp * l.warps_per_cta;
-    const long long slabs = (s.headdim + rows_per_cta - 1) / rows_per_cta;
-    const long long grid = s.batch * s.nheads * slabs;
-    if (grid > INT_MAX) return fail(SSU_ERR_UNSUPPORTED, "grid of %lld CTAs exceeds 2^31", grid);
+    ssu_launch_t l = handle->has_override ? handle->override_launch
+                                          : table_launch(*handle, s, strides);
+    if (l.mode == SSU_MODE_BULK && !bulk_fits(*handle, l, strides)) {
+        if (handle->has_override)
+            return fail(SSU_ERR_UNSUPPORTED,
+                        "BULK mode needs contiguous state rows (row stride 128)");
+        l = ssu_launch_t{SSU_MODE_VEC, 8, 2, 0};
+    }
+    const int rows_per_tile = l.rows_per_warp * l.warps_per_cta;
+    const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
+    const long long tiles = s.batch * s.nheads * slabs;
+    if (tiles > INT_MAX)
+        return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
 
     SsuParams p;
     p.state = state_pool;
@@ -425,17 +824,33 @@ ssu_status_t ssu_update(ssu_handle_t handle, float *state_pool, const void *stat
     p.headdim = static_cast<int>(s.headdim);
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
     p.slabs = static_cast<int>(slabs);
-    p.rows_per_cta = rows_per_cta;
+    p.rows_per_cta = rows_per_tile;
     p.err = handle->err;
 
     DeviceGuard guard(handle->device);
     if (guard.err != cudaSuccess)
         return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e =
-        s.index_dtype == SSU_INDEX_I64
-            ? launch_vec<true>(p, l.rows_per_warp, l.warps_per_cta, (unsigned)grid, cs)
-            : launch_vec<false>(p, l.rows_per_warp, l.warps_per_cta, (unsigned)grid, cs);
+    const bool i64 = s.index_dtype == SSU_INDEX_I64;
+    cudaError_t e;
+    if (l.mode == SSU_MODE_BULK) {
+        const BulkKernel k = bulk_kernel(l.rows_per_warp, i64);
+        const unsigned smem = bulk_smem_bytes(l.stages, rows_per_tile);
+        const int threads = 32 * (1 + l.warps_per_cta);
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
+        if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
+        if (e == cudaSuccess) {
+            const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
+            const unsigned grid = static_cast<unsigned>(tiles < slots ? tiles : slots);
+            const BulkShape q{tiles, l.stages};
+            k<<<grid, threads, smem, cs>>>(p, q);
+            e = cudaGetLastError();
+        }
+    } else {
+        e = i64 ? launch_vec<true>(p, l.rows_per_warp, l.warps_per_cta, (unsigned)tiles, cs)
+                : launch_vec<false>(p, l.rows_per_warp, l.warps_per_cta, (unsigned)tiles, cs);
+    }
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -447,13 +862,16 @@ ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *s
     if (guard.err != cudaSuccess)
         return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
-    unsigned host[2] = {0u, 0xffffffffu};
+    unsigned host[3] = {0u, 0xffffffffu, 0u};
     if (e == cudaSuccess) e = cudaMemcpy(host, handle->err, sizeof(host), cudaMemcpyDeviceToHost);
-    const unsigned init[2] = {0u, 0xffffffffu};
+    const unsigned init[3] = {0u, 0xffffffffu, 0u};
     if (e == cudaSuccess) e = cudaMemcpy(handle->err, init, sizeof(init), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "ssu_get_error: %s", cudaGetErrorString(e));
     if (skipped) *skipped = host[0];
     if (first_bad) *first_bad = host[0] ? static_cast<int64_t>(host[1]) : -1;
+    if (host[2])
+        return fail(SSU_ERR_TIMEOUT, "%u pipeline wait(s) timed out; results are incomplete",
+                    host[2]);
     if (host[0]) return fail(SSU_ERR_INDEX_OOB, "%u request(s) named a slot outside the pool",
                              host[0]);
     return ok();

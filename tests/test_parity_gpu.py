@@ -76,7 +76,10 @@ def test_groups(op, H, G):
     _compare_all(pr, t, pr.pool)
 
 
-SHAPES = [(r, w) for r in (1, 2, 4, 8, 16) for w in (1, 2, 3, 4, 8, 16)]
+VEC_SHAPES = [(ssu.SSU_MODE_VEC, r, w, 0) for r in (1, 2, 4, 8, 16) for w in (1, 2, 3, 4, 8, 16)]
+BULK_SHAPES = [(ssu.SSU_MODE_BULK, r, w, st) for r in (2, 4, 8, 16) for w in (1, 2, 3, 4, 8)
+               for st in (2, 3, 5) if st * r * w * 512 <= 200 * 1024]
+SHAPES = VEC_SHAPES + BULK_SHAPES
 
 
 @pytest.mark.parametrize("P", [64, 40])
@@ -89,15 +92,79 @@ def test_every_launch_shape_is_bitwise_identical(op, P):
     _run(op, ref)
     _compare_all(pr, ref, pr.pool)
     try:
-        for rpw, wpc in SHAPES:
+        for shape in SHAPES:
             t = to_device(pr, DEV)
-            op.set_launch(ssu.SSU_MODE_VEC, rpw, wpc)
+            op.set_launch(*shape)
             _run(op, t)
-            assert torch.equal(t["state_pool"], ref["state_pool"]), (rpw, wpc)
-            assert torch.equal(t["out"].view(torch.int16), ref["out"].view(torch.int16)), \
-                (rpw, wpc)
+            assert torch.equal(t["state_pool"], ref["state_pool"]), shape
+            assert torch.equal(t["out"].view(torch.int16), ref["out"].view(torch.int16)), shape
+        assert op.get_error() == (0, -1)
     finally:
         op.set_launch(ssu.SSU_MODE_AUTO)
+
+
+@pytest.mark.parametrize("shape", [(ssu.SSU_MODE_BULK, 8, 4, 4), (ssu.SSU_MODE_BULK, 2, 1, 2),
+                                   (ssu.SSU_MODE_BULK, 16, 8, 3)])
+@pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
+def test_bulk_pipeline_many_tiles_per_cta(op, shape, idx_dtype):
+    # A batch large enough that every persistent CTA streams many tiles through its ring
+    # (several wraps of every stage), compared with the oracle on sampled requests.
+    bs, H = 96, 16
+    pr = wl.make_problem(bs, H, pool_size=bs + 16, seed=17)
+    t = to_device(pr, DEV, idx_dtype)
+    op.set_launch(*shape)
+    try:
+        _run(op, t)
+        assert op.get_error() == (0, -1)
+    finally:
+        op.set_launch(ssu.SSU_MODE_AUTO)
+    _compare_all(pr, t, pr.pool)
+
+
+def test_bulk_skips_out_of_range_slots(op):
+    pr = wl.make_problem(40, 16, pool_size=48, seed=23)
+    idx = pr.idx.copy()
+    bad = [0, 5, 39]
+    idx[bad] = [48, -1, 1 << 30]
+    t = to_device(pr, DEV)
+    t["state_batch_indices"] = torch.from_numpy(idx).to(DEV).to(torch.int32)
+    t["out"].fill_(3.0)
+    op.set_launch(ssu.SSU_MODE_BULK, 8, 4, 3)
+    try:
+        _run(op, t)
+        assert op.get_error() == (3, 0)
+    finally:
+        op.set_launch(ssu.SSU_MODE_AUTO)
+    good = np.setdiff1d(np.arange(40), bad)
+    assert (t["out"][bad].float() == 3.0).all()
+    ref_states, ref_y = oracle_on_requests(pr.pool, idx, good, pr.x, pr.dt, pr.dt_bias, pr.A,
+                                           pr.B, pr.C, pr.D)
+    got_pool = t["state_pool"].cpu().numpy()
+    check_state(got_pool[idx[good]], ref_states)
+    untouched = np.setdiff1d(np.arange(48), idx[good])
+    assert np.array_equal(got_pool[untouched], pr.pool[untouched])
+    Ch, Dx = expected_terms(pr.x[good], pr.D, pr.C[good], 1, 16)
+    check_y(bits_of(t["out"])[good], ref_y, ref_states, Ch, Dx, 128)
+
+
+def test_bulk_needs_contiguous_rows(op):
+    # rows padded to 132 floats: the bulk copy of a tile would cover the padding, so a forced
+    # BULK shape is refused and the table path (VEC) still gives the right answer.
+    pr = wl.make_problem(4, 16, pool_size=8, seed=29)
+    padded = torch.zeros(8, 16, 64, 132, device=DEV)
+    padded[..., :128] = torch.from_numpy(pr.pool).to(DEV)
+    t = to_device(pr, DEV)
+    t["state_pool"] = padded[..., :128]
+    op.set_launch(ssu.SSU_MODE_BULK, 8, 4, 3)
+    try:
+        with pytest.raises(ssu.SsuError) as e:
+            _run(op, t)
+        assert e.value.status == ssu.SSU_ERR_UNSUPPORTED
+    finally:
+        op.set_launch(ssu.SSU_MODE_AUTO)
+    _run(op, t)
+    _compare_all(pr, dict(t, state_pool=t["state_pool"]), pr.pool)
+    assert (padded[..., 128:] == 0).all()
 
 
 def test_packed_strided_views_and_broadcasts(op):
@@ -169,7 +236,9 @@ def test_invalid_arguments_are_rejected_before_launch(op):
     pr = wl.make_problem(4, 16, pool_size=8, seed=2)
     t = to_device(pr, DEV)
     bad = dict(t)
-    bad["state_pool"] = t["state_pool"][:, :, :, 1:].contiguous()[..., :127]   # dstate 127
+    bad["state_pool"] = torch.zeros(8, 16, 64, 127, device=DEV)                 # dstate 127
+    bad["B"] = torch.zeros(4, 1, 127, dtype=torch.bfloat16, device=DEV)
+    bad["C"] = torch.zeros(4, 1, 127, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(ssu.SsuError) as e:
         _run(op, bad)
     assert e.value.status == ssu.SSU_ERR_UNSUPPORTED

@@ -25,7 +25,10 @@ pytestmark = pytest.mark.gpu
 HEADS = [8, 16, 32, 64, 128]
 BATCHES = list(range(1, 65)) + list(range(72, 1025, 8))
 GUARD = 16
-ALT_SHAPES = [(16, 4), (4, 1), (1, 16), (2, 8), (8, 2), (16, 1), (4, 4), (8, 8)]
+ALT_SHAPES = [(ssu.SSU_MODE_VEC, 16, 4, 0), (ssu.SSU_MODE_BULK, 8, 4, 4),
+              (ssu.SSU_MODE_VEC, 4, 1, 0), (ssu.SSU_MODE_BULK, 4, 2, 3),
+              (ssu.SSU_MODE_VEC, 1, 16, 0), (ssu.SSU_MODE_BULK, 16, 4, 2),
+              (ssu.SSU_MODE_VEC, 8, 2, 0), (ssu.SSU_MODE_BULK, 2, 8, 5)]
 
 
 def test_grid_has_920_points():
@@ -56,12 +59,12 @@ def test_sweep(H):
             pb = master[:n].clone()
             oa = torch.zeros(bs, H, 64, dtype=torch.bfloat16, device="cuda")
             ob = torch.zeros_like(oa)
-            rpw, wpc = ALT_SHAPES[i % len(ALT_SHAPES)]
-            alt.set_launch(ssu.SSU_MODE_VEC, rpw, wpc)
+            shape = ALT_SHAPES[i % len(ALT_SHAPES)]
+            alt.set_launch(*shape)
             op(pa, idx_d, xd, dtd, bias_d, A_d, Bd, Cd, D_d, oa)
             alt(pb, idx_d, xd, dtd, bias_d, A_d, Bd, Cd, D_d, ob)
-            assert torch.equal(pa, pb), (H, bs, rpw, wpc)
-            assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), (H, bs, rpw, wpc)
+            assert torch.equal(pa, pb), (H, bs, shape)
+            assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), (H, bs, shape)
             untouched = np.setdiff1d(np.arange(n), idx)
             ut = torch.from_numpy(untouched).cuda()
             assert torch.equal(pa[ut], master[:n][ut]), (H, bs)
