@@ -2,9 +2,9 @@
  * ssu.h - C ABI of the GB300 (sm_103a) Mamba2 decode-step selective state update.
  *
  * The operation (operands as in sglang PR #41223, Summary and Details / Kernel measurement:
- * "each step it reads and writes every request's fp32 SSM state"; state pool
+ * every decode step loads and stores the fp32 SSM state of every request; state pool
  * [pool, H, 64, 128] fp32 with random state_batch_indices; x [bs, H, 64] and B/C [bs, 1, 128]
- * as strided views of one tensor; dt, A, D and dt_bias as stride-0 broadcasts).  The pages
+ * as views into one shared bf16 tensor; dt, A, D and dt_bias broadcast with stride 0).  The pages
  * never print the arithmetic; this library computes the standard Mamba2 decode step:
  *
  *   for each request b (slot s = state_batch_indices[b]) and head h (group g = h / (H/G)):
@@ -76,7 +76,7 @@ typedef struct {
 
 /*
  * Element strides of every operand, outermost dimension first.  Broadcast operands carry the
- * expanded shapes that the model uses ("head-expanded"), with stride 0 over the expanded
+ * expanded shapes that the model uses (one value per head), with stride 0 over the expanded
  * dimensions; any non-negative outer stride is accepted.
  */
 typedef struct {

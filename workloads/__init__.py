@@ -138,6 +138,6 @@ def packed_xbc(rng: np.random.Generator, bs: int, H: int, P: int = HEADDIM, N: i
     """One packed bf16 tensor ``[bs, H*P + 2*G*N]`` holding x, then B, then C per request.
 
     The strided-view workload (batch 512) takes x, B and C as views into this one tensor,
-    as the kernel measurement of sglang PR #41223 does ("strided views of one tensor").
+    as the kernel measurement of sglang PR #41223 does (Details / Kernel measurement).
     """
     return f32_to_bf16_bits(rng.standard_normal((bs, H * P + 2 * G * N), dtype=np.float32))
