@@ -175,6 +175,37 @@ ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch);
 ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
                             ssu_launch_t *launch);
 
+/*
+ * Allocation-free variant of ssu_update.  No counterpart exists in the paper: it serves
+ * callers that cannot call cudaMalloc, such as code running under an allocator that must not
+ * be re-entered, or a runtime that hands out only memory it owns, and so cannot create a
+ * handle (ssu_create allocates the device counters).  It takes no handle and allocates
+ * nothing: the skipped-request counters the kernel needs live in a fixed 256-byte array in
+ * the library's device memory (SSU_STATIC_SCRATCH_BYTES, held by every GPU that loads the
+ * library until the process exits).
+ *
+ * Arguments are those of ssu_update, on the CURRENT CUDA device, plus:
+ *   counters_out  optional caller-owned DEVICE buffer of 3 uint32: after the kernel the call
+ *                 enqueues a copy of [skipped requests, smallest skipped request index
+ *                 (0xFFFFFFFF if none), 0]; NULL skips the copy.
+ * Each call clears the shared counters, launches the VEC kernel of the built-in table and
+ * copies the counters out, all on `stream`.  The first call on a device looks up the
+ * array's device address (once per device, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array: calls that
+ * overlap on the GPU (different streams, no ordering) race on the counters, so order them.
+ * Batches above SSU_STATIC_MAX_BATCH requests are rejected with SSU_ERR_UNSUPPORTED (the
+ * smallest skipped index is kept in one 32-bit word of the array).  Never calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ */
+#define SSU_STATIC_SCRATCH_BYTES 256
+#define SSU_STATIC_MAX_BATCH 2147483647LL
+ssu_status_t ssu_update_static(float *state_pool, const void *state_batch_indices,
+                               const uint16_t *x, const uint16_t *dt, const float *dt_bias,
+                               const float *A, const uint16_t *B, const uint16_t *C,
+                               const float *D, uint16_t *out, const ssu_shape_t *shape,
+                               const ssu_strides_t *strides, uint32_t *counters_out,
+                               ssu_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

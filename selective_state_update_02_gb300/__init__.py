@@ -81,7 +81,12 @@ _EXPORTS = {
     "ssu_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_launch_t)]),
     "ssu_get_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_shape_t),
                                       ctypes.POINTER(ssu_launch_t)]),
+    "ssu_update_static": (ctypes.c_int, [_vp] * 10 + [ctypes.POINTER(ssu_shape_t),
+                                                      ctypes.POINTER(ssu_strides_t), _vp, _vp]),
 }
+
+SSU_STATIC_SCRATCH_BYTES = 256
+SSU_STATIC_MAX_BATCH = 2147483647
 
 
 def lib() -> ctypes.CDLL:
@@ -233,6 +238,22 @@ def ssu_update(handle: int, state_pool, state_batch_indices, x, dt, dt_bias, A, 
     ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)]
     _check(lib().ssu_update(handle, *ptrs, ctypes.byref(shape), ctypes.byref(strides),
                             _stream_ptr(stream)), "ssu_update")
+
+
+def ssu_update_static(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out,
+                      counters_out=None, stream=None) -> None:
+    """Allocation-free ssu_update on the current device (no handle).
+
+    For callers that cannot allocate device memory: the kernel's counters live in a fixed
+    256-byte array inside the library.  ``counters_out`` is an optional caller-owned int32/uint32
+    device tensor of >= 3 elements that receives [skipped, smallest skipped index or
+    0xFFFFFFFF, 0].  Calls that overlap on the GPU race on the shared counters.
+    """
+    shape, strides = describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)
+    ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)]
+    _check(lib().ssu_update_static(*ptrs, ctypes.byref(shape), ctypes.byref(strides),
+                                   _ptr(counters_out), _stream_ptr(stream)),
+           "ssu_update_static")
 
 
 def ssu_update_raw(handle: int, ptrs, shape: ssu_shape_t, strides: ssu_strides_t,

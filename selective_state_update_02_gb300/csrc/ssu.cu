@@ -38,6 +38,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "ssu.h"
@@ -878,3 +879,127 @@ ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *s
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free entry point: the kernel's counters live in a fixed device array.
+
+static __device__ __align__(256) unsigned ssu_static_scratch[SSU_STATIC_SCRATCH_BYTES / 4];
+
+namespace {
+
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mutex;
+unsigned *g_static_addr[kStaticMaxDevices] = {};
+int g_static_sms[kStaticMaxDevices] = {};
+
+// Device address of the array on the current device `dev`, looked up once per device.
+ssu_status_t static_scratch_on(int dev, unsigned **addr, int *sms) {
+    if (dev < 0 || dev >= kStaticMaxDevices)
+        return fail(SSU_ERR_UNSUPPORTED, "device %d is beyond the %d devices supported", dev,
+                    kStaticMaxDevices);
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_addr[dev]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, ssu_static_scratch);
+        if (e != cudaSuccess)
+            return fail(SSU_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return fail(SSU_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        g_static_sms[dev] = n;
+        g_static_addr[dev] = static_cast<unsigned *>(ptr);
+    }
+    *addr = g_static_addr[dev];
+    *sms = g_static_sms[dev];
+    return SSU_OK;
+}
+
+}  // namespace
+
+extern "C" ssu_status_t ssu_update_static(float *state_pool, const void *state_batch_indices,
+                                          const uint16_t *x, const uint16_t *dt,
+                                          const float *dt_bias, const float *A,
+                                          const uint16_t *B, const uint16_t *C, const float *D,
+                                          uint16_t *out, const ssu_shape_t *shape,
+                                          const ssu_strides_t *strides, uint32_t *counters_out,
+                                          ssu_stream_t stream) {
+    if (shape && shape->batch > SSU_STATIC_MAX_BATCH)
+        return fail(SSU_ERR_UNSUPPORTED,
+                    "batch %lld exceeds SSU_STATIC_MAX_BATCH (%lld): the static counters keep "
+                    "the smallest skipped request in 32 bits",
+                    (long long)shape->batch, (long long)SSU_STATIC_MAX_BATCH);
+    ssu_status_t st = validate_impl(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C,
+                                    D, out, shape, strides);
+    if (st != SSU_OK || shape->batch == 0) return st;
+    if (counters_out && !aligned(counters_out, 4))
+        return fail(SSU_ERR_MISALIGNED, "counters_out is not 4-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    unsigned *scratch = nullptr;
+    int sms = 0;
+    st = static_scratch_on(dev, &scratch, &sms);
+    if (st != SSU_OK) return st;
+
+    const ssu_shape_t &s = *shape;
+    ssu_handle_s table_only;
+    table_only.sm_count = sms;
+    ssu_launch_t l = table_launch(table_only, s, strides);
+    if (l.mode != SSU_MODE_VEC) l = ssu_launch_t{SSU_MODE_VEC, 8, 2, 0};
+    const int rows_per_tile = l.rows_per_warp * l.warps_per_cta;
+    const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
+    const long long tiles = s.batch * s.nheads * slabs;
+    if (tiles > INT_MAX) return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
+
+    SsuParams p;
+    p.state = state_pool;
+    p.idx = state_batch_indices;
+    p.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    p.dt = reinterpret_cast<const __nv_bfloat16 *>(dt);
+    p.dt_bias = dt_bias;
+    p.A = A;
+    p.B = reinterpret_cast<const __nv_bfloat16 *>(B);
+    p.C = reinterpret_cast<const __nv_bfloat16 *>(C);
+    p.D = D;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.st_pool = strides->state[0];
+    p.st_head = strides->state[1];
+    p.st_row = strides->state[2];
+    p.x_b = strides->x[0];
+    p.x_h = strides->x[1];
+    p.out_b = strides->out[0];
+    p.out_h = strides->out[1];
+    p.dt_b = strides->dt[0];
+    p.dt_h = strides->dt[1];
+    p.B_b = strides->B[0];
+    p.B_g = strides->B[1];
+    p.C_b = strides->C[0];
+    p.C_g = strides->C[1];
+    p.bias_h = strides->dt_bias[0];
+    p.D_h = strides->D[0];
+    p.A_h = strides->A[0];
+    p.idx_s = strides->idx;
+    p.pool_size = s.pool_size;
+    p.nheads = static_cast<int>(s.nheads);
+    p.headdim = static_cast<int>(s.headdim);
+    p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
+    p.slabs = static_cast<int>(slabs);
+    p.rows_per_cta = rows_per_tile;
+    p.err = scratch;
+
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // The counters start every call at {0 skipped, no smallest index (all ones), 0 timeouts}.
+    e = cudaMemsetAsync(scratch, 0, 3 * sizeof(unsigned), cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scratch + 1, 0xff, sizeof(unsigned), cs);
+    if (e == cudaSuccess)
+        e = s.index_dtype == SSU_INDEX_I64
+                ? launch_vec<true>(p, l.rows_per_warp, l.warps_per_cta, (unsigned)tiles, cs)
+                : launch_vec<false>(p, l.rows_per_warp, l.warps_per_cta, (unsigned)tiles, cs);
+    if (e == cudaSuccess && counters_out)
+        e = cudaMemcpyAsync(counters_out, scratch, 3 * sizeof(unsigned),
+                            cudaMemcpyDeviceToDevice, cs);
+    if (e != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "ssu_update_static: %s", cudaGetErrorString(e));
+    return ok();
+}
