@@ -45,7 +45,8 @@ SERVING_SETS = 19            # 2432 slots at batch 128
 NOMINAL_HBM_GBS = 8000.0     # the pages' round GB200/B200 HBM3e figure
 FALLBACK_HBM_GBS = 6800.0
 PAGE_US = {8: 4.02, 128: 24.1, 512: 85.7}   # sglang PR #41223 Speedup Result, B200 (context)
-KERNEL_SOURCE = ROOT / "selective_state_update_02_gb300" / "csrc" / "ssu.cu"
+CSRC = ROOT / "selective_state_update_02_gb300" / "csrc"
+KERNEL_SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_device.cuh"]
 
 
 # ---- arithmetic of the measurement (host logic, tested on CPU) ---------------------------
@@ -84,8 +85,13 @@ def load_peaks() -> dict:
     return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
-def source_digest() -> str:
-    return hashlib.sha256(KERNEL_SOURCE.read_bytes()).hexdigest()[:16]
+def source_digest(files=None) -> str:
+    """Digest of the sources that define the timed kernel (its translation unit and the
+    device header it includes): counters taken on other sources are not reported."""
+    h = hashlib.sha256()
+    for f in files or KERNEL_SOURCES:
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload_tag: str) -> int | None:
@@ -446,6 +452,8 @@ def run_ours(args) -> None:
     ssu.lib()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     handle = ssu.ssu_create(local)
+    if args.launch:
+        ssu.ssu_set_launch(handle, *[int(v) for v in args.launch.split(",")])
     warmup = max(args.warmup, 3)
     bs = args.batch
     main = Workload(bs, NHEADS, dev, seed=rank, l2_bytes=l2, packed=True)
@@ -464,9 +472,9 @@ def run_ours(args) -> None:
     peaks = load_peaks()
     bpc = bytes_per_call(bs)
     achieved_gbs = bpc / (per_launch_us * 1e-6) / 1e9
-    tag = f"batch{bs}"
-    traffic = recorded_traffic(tag)
     launch = ssu.ssu_get_launch(handle, main.args[0][1])
+    tag = f"batch{bs}" + ("-bulk" if launch[0] == 2 else "")
+    traffic = recorded_traffic(tag)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": untimed, "ms_per_step": round(value / 1000.0, 6),
@@ -484,10 +492,18 @@ def run_ours(args) -> None:
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": bpc,
-                     "peak_source": peaks["source"], "kernel": "ssu_vec_kernel"},
+                     "peak_source": peaks["source"],
+                     "kernel": "ssu_bulk_kernel" if launch[0] == 2 else "ssu_vec_kernel"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if not args.skip_ceiling:
+        state_bytes = bs * NHEADS * HEADDIM * DSTATE * 4
+        t_in = same_size_ceiling(state_bytes, dev, l2)
+        ceil_gbs = 2 * state_bytes / (t_in * 1e-6) / 1e9
+        line["roofline"]["same_size_inplace_gbs"] = round(ceil_gbs, 1)
+        line["roofline"]["frac_of_same_size_inplace"] = round(
+            (2 * state_bytes / (per_launch_us * 1e-6) / 1e9) / ceil_gbs, 4)
     if not args.skip_extra and world == 1:
         by = {}
         for b in (8, 128, 512):
@@ -523,6 +539,66 @@ def _smi_index(local: int) -> int:
         if local < len(parts) and parts[local].strip().isdigit():
             return int(parts[local])
     return local
+
+
+def graph_time_us(fn, n_sets: int, calls: int = 400, reps: int = 3) -> float:
+    """Best-of-`reps` time per call of `fn(i % n_sets)` replayed from one CUDA graph."""
+    import torch
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(n_sets):
+            fn(i)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(calls):
+            fn(i % n_sets)
+    g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1000.0 / calls)
+    return best
+
+
+def same_size_ceiling(nbytes: int, dev, l2_bytes: int, copy: bool = False) -> float:
+    """µs per call of PyTorch's own in-place elementwise kernel (`mul_`, read + write of
+    `nbytes`) or, with `copy`, of `copy_` between two buffers, over buffers rotated across
+    at least 3x the L2: the rate a library kernel reaches at this call size."""
+    import torch
+    n_sets = max(3, -(-3 * l2_bytes // nbytes))
+    bufs = [torch.randn(nbytes // 4, device=dev) for _ in range(n_sets)]
+    if copy:
+        dst = [torch.empty_like(b) for b in bufs]
+        us = graph_time_us(lambda i: dst[i].copy_(bufs[i]), n_sets)
+        del dst
+    else:
+        us = graph_time_us(lambda i: bufs[i].mul_(1.0000001), n_sets)
+    del bufs
+    torch.cuda.empty_cache()
+    return us
+
+
+def run_calibrate(args) -> None:
+    """Library copy / in-place rates at the decode step's state sizes (batch 8, 128, 512)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    for bs in (8, 128, 512):
+        nbytes = bs * NHEADS * HEADDIM * DSTATE * 4
+        t_copy = same_size_ceiling(nbytes, dev, l2, copy=True)
+        t_rmw = same_size_ceiling(nbytes, dev, l2)
+        print(json.dumps({"batch": bs, "state_MiB": nbytes >> 20,
+                          "copy_us": round(t_copy, 3),
+                          "copy_tbps": round(2 * nbytes / t_copy / 1e6, 3),
+                          "inplace_us": round(t_rmw, 3),
+                          "inplace_tbps": round(2 * nbytes / t_rmw / 1e6, 3)}), flush=True)
 
 
 SWEEP_SHAPES = ([(1, r, w, 0) for r in (1, 2, 4, 8, 16) for w in (1, 2, 4, 8)] +
@@ -577,14 +653,23 @@ def main() -> None:
     ap.add_argument("--skip-extra", action="store_true", help="skip the batch 8/512 lines")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--launch", default="",
+                    help="force a launch shape 'mode,rows_per_warp,warps_per_cta,stages' "
+                         "(mode 1 = VEC, 2 = BULK) instead of the built-in table")
     ap.add_argument("--sweep", action="store_true", help="launch-shape sweep instead")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="library copy / in-place rates at the call sizes instead")
+    ap.add_argument("--skip-ceiling", action="store_true",
+                    help="skip the same-size in-place ceiling measurement")
     ap.add_argument("--sweep-batches", type=int, nargs="+", default=[8, 128, 512])
     ap.add_argument("--sweep-us-budget", type=float, default=60000.0,
                     help="approximate GPU time per sweep point, microseconds")
     args = ap.parse_args()
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
-    if args.sweep:
+    if args.calibrate:
+        run_calibrate(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -1,4 +1,5 @@
-"""Builds libssu.so in-tree with nvcc for sm_103a (one translation unit, one -gencode)."""
+"""Builds libssu.so in-tree with nvcc for sm_103a (one -gencode; the translation units are
+compiled in parallel, then linked into one shared library)."""
 
 from __future__ import annotations
 
@@ -9,8 +10,10 @@ from pathlib import Path
 
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
-SOURCES = [PKG / "csrc" / "ssu.cu"]
-HEADERS = [ROOT / "include" / "ssu.h"]
+CSRC = PKG / "csrc"
+SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_host.cpp"]
+HEADERS = [ROOT / "include" / "ssu.h", CSRC / "ssu_device.cuh", CSRC / "ssu_host.h"]
+OBJDIR = PKG / "_build"
 LIB = PKG / "libssu.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -22,10 +25,14 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libssu.so")
 
 
-def nvcc_command(out: Path, extra: list[str] | None = None) -> list[str]:
+def compile_command(src: Path, obj: Path, extra: list[str] | None = None) -> list[str]:
     return [nvcc_path(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-            "-shared", "-I", str(ROOT / "include"), *(extra or []),
-            *[str(s) for s in SOURCES], "-o", str(out)]
+            "-I", str(ROOT / "include"), "-I", str(CSRC), *(extra or []), "-c", str(src),
+            "-o", str(obj)]
+
+
+def link_command(objs: list[Path], out: Path) -> list[str]:
+    return [nvcc_path(), *ARCH, "-shared", *[str(o) for o in objs], "-o", str(out)]
 
 
 def stale() -> bool:
@@ -37,8 +44,16 @@ def stale() -> bool:
 
 def build(force: bool = False, extra: list[str] | None = None) -> Path:
     """Compile libssu.so next to this file unless it is up to date."""
-    if force or stale():
-        tmp = LIB.with_name(f"libssu.so.tmp{os.getpid()}")
-        subprocess.run(nvcc_command(tmp, extra), check=True)
-        os.replace(tmp, LIB)
+    if not (force or stale()):
+        return LIB
+    OBJDIR.mkdir(exist_ok=True)
+    objs = [OBJDIR / (src.name + ".o") for src in SOURCES]
+    procs = [subprocess.Popen(compile_command(src, obj, extra))
+             for src, obj in zip(SOURCES, objs)]
+    codes = [p.wait() for p in procs]
+    if any(codes):
+        raise subprocess.CalledProcessError(max(codes), "nvcc (libssu sources)")
+    tmp = LIB.with_name(f"libssu.so.tmp{os.getpid()}")
+    subprocess.run(link_command(objs, tmp), check=True)
+    os.replace(tmp, LIB)
     return LIB

@@ -34,123 +34,20 @@
 #include <cuda_runtime.h>
 
 #include <climits>
-#include <cstdarg>
 #include <cstdint>
-#include <cstdio>
-#include <cstring>
 #include <mutex>
-#include <string>
 
 #include "ssu.h"
+#include "ssu_device.cuh"
+#include "ssu_host.h"
+
+using ssu_host::aligned;
+using ssu_host::DeviceGuard;
+using ssu_host::fail;
+using ssu_host::ok;
+using ssu_host::validate_impl;
 
 namespace {
-
-constexpr int kDstate = 128;             // dstate this build implements: 32 lanes x 4 columns
-constexpr int kRowBytes = kDstate * 4;   // one fp32 state row
-constexpr int kMaxWarpsPerCta = 16;      // VEC
-constexpr int kMaxBulkWarps = 8;         // BULK compute warps (plus one producer warp)
-constexpr int kMaxStages = 8;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per mbarrier wait
-
-// Everything one launch needs, passed by value in the kernel parameter space.
-struct SsuParams {
-    float *state;
-    const void *idx;
-    const __nv_bfloat16 *x;
-    const __nv_bfloat16 *dt;
-    const float *dt_bias;
-    const float *A;
-    const __nv_bfloat16 *B;
-    const __nv_bfloat16 *C;
-    const float *D;
-    __nv_bfloat16 *out;
-    long long st_pool, st_head, st_row;  // state strides (elements); dstate stride is 1
-    long long x_b, x_h, out_b, out_h, dt_b, dt_h;
-    long long B_b, B_g, C_b, C_g;
-    long long bias_h, D_h, A_h, idx_s;
-    long long pool_size;
-    int nheads, headdim, heads_per_group;
-    int slabs;         // tiles per (request, head) unit
-    int rows_per_cta;  // rows per tile
-    unsigned *err;     // [0] skipped requests, [1] smallest skipped request, [2] timeouts
-};
-
-// BULK launch geometry.
-struct BulkShape {
-    long long tiles;  // batch * nheads * slabs
-    int stages;
-};
-
-__device__ __forceinline__ float softplus_f32(float z) {
-    // log(1 + e^z); above 20 the correction is below fp32 resolution of z.
-    return z > 20.0f ? z : log1pf(expf(z));
-}
-
-// The update of one lane's 4 columns of one row; returns the lane's part of the readout.
-__device__ __forceinline__ float update_cols(float4 &w, float dA, float k, const float (&bb)[4],
-                                             const float (&cc)[4]) {
-    w.x = fmaf(w.x, dA, k * bb[0]);
-    w.y = fmaf(w.y, dA, k * bb[1]);
-    w.z = fmaf(w.z, dA, k * bb[2]);
-    w.w = fmaf(w.w, dA, k * bb[3]);
-    float part = w.x * cc[0];
-    part = fmaf(w.y, cc[1], part);
-    part = fmaf(w.z, cc[2], part);
-    part = fmaf(w.w, cc[3], part);
-    return part;
-}
-
-// Sums R per-lane parts (one per row) over the 32 lanes.  The pairs are always formed by xor
-// masks 16, 8, 4, 2, 1 in that order (the tree of a plain butterfly), but while a lane holds
-// more than one row it hands half of its rows to its partner at each step ("reduce-scatter"),
-// which needs R - 1 + (5 - log2 R) shuffles instead of 5 R.  Each sum is the same IEEE value the
-// plain butterfly gives (a + b == b + a exactly), whatever R is.  Afterwards lane l holds the
-// total of row row_of_lane<R>(l).
-template <int R>
-__device__ __forceinline__ float reduce_rows(float (&v)[R], int lane) {
-    static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
-#pragma unroll
-    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int j = 0; j < n / 2; ++j) {
-            const float give = upper ? v[j] : v[j + n / 2];
-            const float keep = upper ? v[j + n / 2] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, give, m);
-        }
-    }
-    float t = v[0];
-#pragma unroll
-    for (int m = 16 / R; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
-    return t;
-}
-
-// The row whose total lane l holds after reduce_rows<R>.
-template <int R>
-__device__ __forceinline__ int row_of_lane(int lane) {
-    int row = 0;
-#pragma unroll
-    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1)
-        if (lane & m) row += n / 2;
-    return row;
-}
-
-// Lanes that write a readout: one per group of lanes holding the same row.
-template <int R>
-__device__ __forceinline__ bool writes_row(int lane) {
-    return (lane & (32 / R - 1)) == 0;
-}
-
-template <bool kIdx64>
-__device__ __forceinline__ long long load_slot(const SsuParams &p, long long b) {
-    if (kIdx64) return __ldg(static_cast<const long long *>(p.idx) + b * p.idx_s);
-    return static_cast<long long>(__ldg(static_cast<const int *>(p.idx) + b * p.idx_s));
-}
-
-__device__ __forceinline__ void record_skip(const SsuParams &p, long long b) {
-    atomicAdd(&p.err[0], 1u);
-    atomicMin(&p.err[1], static_cast<unsigned>(b));
-}
 
 // ---------------------------------------------------------------------------------------
 // VEC kernel
@@ -215,70 +112,6 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         const float xr = __bfloat162float(xp[rl]);
         p.out[b * p.out_b + h * p.out_h + row0 + rl] = __float2bfloat16_rn(fmaf(Dh, xr, total));
     }
-}
-
-// ---------------------------------------------------------------------------------------
-// BULK kernel: PTX helpers (mbarrier, bulk asynchronous copies, proxy fence)
-
-__device__ __forceinline__ unsigned smem_u32(const void *ptr) {
-    return static_cast<unsigned>(__cvta_generic_to_shared(ptr));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
-    unsigned done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase of `parity` to complete; false after kWaitLimitNs without completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int k = 0; k < 32; ++k)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, unsigned bytes,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_mbarrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
 // Shared-memory layout of the BULK kernel: barriers and per-stage slots, then the stages.
@@ -521,107 +354,6 @@ unsigned bulk_smem_bytes(int stages, int tile_rows) {
     return bulk_header_bytes(stages) + static_cast<unsigned>(stages) * tile_rows * kRowBytes;
 }
 
-// ---------------------------------------------------------------------------------------
-// Host side: errors, validation, launch-shape table.
-
-thread_local std::string g_last_error;
-
-ssu_status_t fail(ssu_status_t status, const char *fmt, ...) {
-    char buf[512];
-    va_list ap;
-    va_start(ap, fmt);
-    vsnprintf(buf, sizeof(buf), fmt, ap);
-    va_end(ap);
-    g_last_error = buf;
-    return status;
-}
-
-ssu_status_t ok() {
-    g_last_error.clear();
-    return SSU_OK;
-}
-
-bool aligned(const void *ptr, unsigned bytes) {
-    return (reinterpret_cast<unsigned long long>(ptr) % bytes) == 0;
-}
-
-// Restores the caller's current device on scope exit.
-struct DeviceGuard {
-    int prev = -1;
-    bool switched = false;
-    cudaError_t err = cudaSuccess;
-    explicit DeviceGuard(int dev) {
-        err = cudaGetDevice(&prev);
-        if (err == cudaSuccess && prev != dev) {
-            err = cudaSetDevice(dev);
-            switched = (err == cudaSuccess);
-        }
-    }
-    ~DeviceGuard() {
-        if (switched) cudaSetDevice(prev);
-    }
-};
-
-ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint16_t *x,
-                           const uint16_t *dt, const float *dt_bias, const float *A,
-                           const uint16_t *B, const uint16_t *C, const float *D,
-                           const uint16_t *out, const ssu_shape_t *shape,
-                           const ssu_strides_t *st) {
-    if (!shape || !st) return fail(SSU_ERR_INVALID_ARG, "shape and strides must not be NULL");
-    const ssu_shape_t &s = *shape;
-    if (s.batch < 0) return fail(SSU_ERR_INVALID_ARG, "batch %lld < 0", (long long)s.batch);
-    if (s.nheads < 1 || s.headdim < 1 || s.dstate < 1 || s.ngroups < 1)
-        return fail(SSU_ERR_INVALID_ARG, "nheads, headdim, dstate and ngroups must be >= 1");
-    if (s.pool_size < 0) return fail(SSU_ERR_INVALID_ARG, "pool_size < 0");
-    if (s.nheads % s.ngroups != 0)
-        return fail(SSU_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
-                    (long long)s.nheads, (long long)s.ngroups);
-    if (s.index_dtype != SSU_INDEX_I32 && s.index_dtype != SSU_INDEX_I64)
-        return fail(SSU_ERR_INVALID_ARG, "index_dtype %d is neither I32 nor I64", s.index_dtype);
-    if (s.dstate != kDstate)
-        return fail(SSU_ERR_UNSUPPORTED, "dstate %lld: this build implements dstate 128",
-                    (long long)s.dstate);
-    if (s.headdim > (1 << 20) || s.nheads > (1 << 20))
-        return fail(SSU_ERR_UNSUPPORTED, "headdim and nheads are limited to 2^20");
-    if (s.batch == 0) return ok();  // nothing is read or written: strides are irrelevant
-
-    const int64_t *all[] = {st->state, st->x, st->out, st->dt, st->B, st->C,
-                            st->dt_bias, st->D, st->A};
-    const int lens[] = {4, 3, 3, 3, 3, 3, 2, 2, 3};
-    for (int i = 0; i < 9; ++i)
-        for (int j = 0; j < lens[i]; ++j)
-            if (all[i][j] < 0) return fail(SSU_ERR_INVALID_ARG, "negative stride");
-    if (st->idx < 0) return fail(SSU_ERR_INVALID_ARG, "negative index stride");
-    if (st->state[3] != 1) return fail(SSU_ERR_UNSUPPORTED, "state dstate-stride must be 1");
-    if (st->x[2] != 1) return fail(SSU_ERR_UNSUPPORTED, "x headdim-stride must be 1");
-    if (st->out[2] != 1) return fail(SSU_ERR_UNSUPPORTED, "out headdim-stride must be 1");
-    if (st->B[2] != 1 || st->C[2] != 1)
-        return fail(SSU_ERR_UNSUPPORTED, "B and C dstate-stride must be 1");
-    if (st->dt[2] != 0) return fail(SSU_ERR_UNSUPPORTED, "dt must be constant over headdim");
-    if (st->dt_bias[1] != 0 || st->D[1] != 0)
-        return fail(SSU_ERR_UNSUPPORTED, "dt_bias and D must be constant over headdim");
-    if (st->A[1] != 0 || st->A[2] != 0)
-        return fail(SSU_ERR_UNSUPPORTED, "A must be constant over headdim and dstate");
-    for (int j = 0; j < 3; ++j)
-        if (st->state[j] % 4 != 0)
-            return fail(SSU_ERR_MISALIGNED, "state stride %d (%lld) is not a multiple of 4 floats",
-                        j, (long long)st->state[j]);
-
-    if (!state_pool || !idx || !x || !dt || !dt_bias || !A || !B || !C || !D || !out)
-        return fail(SSU_ERR_INVALID_ARG, "a data pointer is NULL");
-    if (!aligned(state_pool, 16))
-        return fail(SSU_ERR_MISALIGNED, "state_pool is not 16-byte aligned");
-    if (!aligned(idx, s.index_dtype == SSU_INDEX_I64 ? 8 : 4))
-        return fail(SSU_ERR_MISALIGNED, "state_batch_indices is not aligned to its type");
-    if (!aligned(x, 2) || !aligned(dt, 2) || !aligned(B, 2) || !aligned(C, 2) || !aligned(out, 2))
-        return fail(SSU_ERR_MISALIGNED, "a bf16 operand is not 2-byte aligned");
-    if (!aligned(dt_bias, 4) || !aligned(A, 4) || !aligned(D, 4))
-        return fail(SSU_ERR_MISALIGNED, "an fp32 operand is not 4-byte aligned");
-    if (s.batch > INT_MAX / s.nheads)
-        return fail(SSU_ERR_UNSUPPORTED, "batch * nheads exceeds 2^31");
-    return ok();
-}
-
 bool is_pow2_rows(int r, int lo, int hi) {
     return r >= lo && r <= hi && (r & (r - 1)) == 0;
 }
@@ -639,25 +371,19 @@ bool launch_shape_ok(const ssu_launch_t &l) {
 
 }  // namespace
 
-struct ssu_handle_s {
-    int device = 0;
-    int sm_count = 0;
-    int smem_optin = 0;       // max dynamic shared memory per CTA (bytes)
-    unsigned *err = nullptr;  // device: [0] skipped, [1] smallest skipped request, [2] timeouts
-    bool has_override = false;
-    ssu_launch_t override_launch{};
-};
-
 namespace {
 
-// Built-in launch-shape table (measured on GB300 with the cold-L2 rotation workloads).
+// Built-in launch-shape table, from the cold-L2 sweep on GB300 (bench.py --sweep): the VEC
+// kernel with 8 rows per warp (8 x 16-byte loads in flight per thread) is fastest at batch 8,
+// 128 and 512, and 1 to 4 warps per CTA are within 0.2% of each other; 2 warps is used.  For
+// a headdim below 16 the tile shrinks to the largest power of two that fits.
 ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
-    ssu_launch_t l{SSU_MODE_VEC, 8, 1, 0};
-    const long long rows = s.batch * s.nheads * s.headdim;
-    const long long warps_needed = (rows + 7) / 8;
-    if (warps_needed >= 16LL * hd.sm_count) l.warps_per_cta = 2;
+    (void)hd;
     (void)st;
-    return l;
+    int rpw = 8;
+    while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
+    const int wpc = s.headdim >= 2 * rpw ? 2 : 1;
+    return ssu_launch_t{SSU_MODE_VEC, rpw, wpc, 0};
 }
 
 // Whether the BULK kernel can run this call (contiguous rows; shared memory fits).
@@ -670,23 +396,6 @@ bool bulk_fits(const ssu_handle_s &hd, const ssu_launch_t &l, const ssu_strides_
 }  // namespace
 
 extern "C" {
-
-int32_t ssu_abi_version(void) { return SSU_ABI_VERSION; }
-
-const char *ssu_status_string(ssu_status_t status) {
-    switch (status) {
-        case SSU_OK: return "SSU_OK";
-        case SSU_ERR_INVALID_ARG: return "SSU_ERR_INVALID_ARG";
-        case SSU_ERR_UNSUPPORTED: return "SSU_ERR_UNSUPPORTED";
-        case SSU_ERR_MISALIGNED: return "SSU_ERR_MISALIGNED";
-        case SSU_ERR_CUDA: return "SSU_ERR_CUDA";
-        case SSU_ERR_INDEX_OOB: return "SSU_ERR_INDEX_OOB";
-        case SSU_ERR_TIMEOUT: return "SSU_ERR_TIMEOUT";
-    }
-    return "SSU_ERR_UNKNOWN";
-}
-
-const char *ssu_last_error(void) { return g_last_error.c_str(); }
 
 ssu_status_t ssu_create(ssu_handle_t *out, int32_t device) {
     if (!out) return fail(SSU_ERR_INVALID_ARG, "out must not be NULL");

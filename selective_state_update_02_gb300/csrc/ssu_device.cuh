@@ -1,0 +1,184 @@
+// Device-side pieces shared by the decode-step kernels: launch constants, the parameter block,
+// the per-element arithmetic, the readout reduction, slot lookup, and the mbarrier / bulk-copy
+// PTX wrappers.  Included by each kernel translation unit (internal linkage per unit).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace {
+
+constexpr int kDstate = 128;             // dstate this build implements: 32 lanes x 4 columns
+constexpr int kRowBytes = kDstate * 4;   // one fp32 state row
+constexpr int kMaxWarpsPerCta = 16;      // VEC
+constexpr int kMaxBulkWarps = 8;         // BULK compute warps (plus one producer warp)
+constexpr int kMaxStages = 8;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per mbarrier wait
+
+// Everything one launch needs, passed by value in the kernel parameter space.
+struct SsuParams {
+    float *state;
+    const void *idx;
+    const __nv_bfloat16 *x;
+    const __nv_bfloat16 *dt;
+    const float *dt_bias;
+    const float *A;
+    const __nv_bfloat16 *B;
+    const __nv_bfloat16 *C;
+    const float *D;
+    __nv_bfloat16 *out;
+    long long st_pool, st_head, st_row;  // state strides (elements); dstate stride is 1
+    long long x_b, x_h, out_b, out_h, dt_b, dt_h;
+    long long B_b, B_g, C_b, C_g;
+    long long bias_h, D_h, A_h, idx_s;
+    long long pool_size;
+    int nheads, headdim, heads_per_group;
+    int slabs;         // tiles per (request, head) unit
+    int rows_per_cta;  // rows per tile
+    unsigned *err;     // [0] skipped requests, [1] smallest skipped request, [2] timeouts
+};
+
+// BULK launch geometry.
+struct BulkShape {
+    long long tiles;  // batch * nheads * slabs
+    int stages;
+};
+
+__device__ __forceinline__ float softplus_f32(float z) {
+    // log(1 + e^z); above 20 the correction is below fp32 resolution of z.
+    return z > 20.0f ? z : log1pf(expf(z));
+}
+
+// The update of one lane's 4 columns of one row; returns the lane's part of the readout.
+__device__ __forceinline__ float update_cols(float4 &w, float dA, float k, const float (&bb)[4],
+                                             const float (&cc)[4]) {
+    w.x = fmaf(w.x, dA, k * bb[0]);
+    w.y = fmaf(w.y, dA, k * bb[1]);
+    w.z = fmaf(w.z, dA, k * bb[2]);
+    w.w = fmaf(w.w, dA, k * bb[3]);
+    float part = w.x * cc[0];
+    part = fmaf(w.y, cc[1], part);
+    part = fmaf(w.z, cc[2], part);
+    part = fmaf(w.w, cc[3], part);
+    return part;
+}
+
+// Sums R per-lane parts (one per row) over the 32 lanes.  The pairs are always formed by xor
+// masks 16, 8, 4, 2, 1 in that order (the tree of a plain butterfly), but while a lane holds
+// more than one row it hands half of its rows to its partner at each step ("reduce-scatter"),
+// which needs R - 1 + (5 - log2 R) shuffles instead of 5 R.  Each sum is the same IEEE value the
+// plain butterfly gives (a + b == b + a exactly), whatever R is.  Afterwards lane l holds the
+// total of row row_of_lane<R>(l).
+template <int R>
+__device__ __forceinline__ float reduce_rows(float (&v)[R], int lane) {
+    static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
+#pragma unroll
+    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const float give = upper ? v[j] : v[j + n / 2];
+            const float keep = upper ? v[j + n / 2] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int m = 16 / R; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+    return t;
+}
+
+// The row whose total lane l holds after reduce_rows<R>.
+template <int R>
+__device__ __forceinline__ int row_of_lane(int lane) {
+    int row = 0;
+#pragma unroll
+    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1)
+        if (lane & m) row += n / 2;
+    return row;
+}
+
+// Lanes that write a readout: one per group of lanes holding the same row.
+template <int R>
+__device__ __forceinline__ bool writes_row(int lane) {
+    return (lane & (32 / R - 1)) == 0;
+}
+
+template <bool kIdx64>
+__device__ __forceinline__ long long load_slot(const SsuParams &p, long long b) {
+    if (kIdx64) return __ldg(static_cast<const long long *>(p.idx) + b * p.idx_s);
+    return static_cast<long long>(__ldg(static_cast<const int *>(p.idx) + b * p.idx_s));
+}
+
+__device__ __forceinline__ void record_skip(const SsuParams &p, long long b) {
+    atomicAdd(&p.err[0], 1u);
+    atomicMin(&p.err[1], static_cast<unsigned>(b));
+}
+
+// ---------------------------------------------------------------------------------------
+// BULK kernel: PTX helpers (mbarrier, bulk asynchronous copies, proxy fence)
+
+__device__ __forceinline__ unsigned smem_u32(const void *ptr) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `parity` to complete; false after kWaitLimitNs without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 32; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, unsigned bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+}  // namespace

@@ -1,0 +1,118 @@
+// Host-side helpers of libssu: error messages, argument validation, status names.
+
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "ssu_host.h"
+
+namespace ssu_host {
+
+constexpr int kDstate = 128;  // dstate this build implements
+
+namespace {
+thread_local std::string g_last_error;
+}  // namespace
+
+ssu_status_t fail(ssu_status_t status, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+ssu_status_t ok() {
+    g_last_error.clear();
+    return SSU_OK;
+}
+
+bool aligned(const void *ptr, unsigned bytes) {
+    return (reinterpret_cast<unsigned long long>(ptr) % bytes) == 0;
+}
+
+ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint16_t *x,
+                           const uint16_t *dt, const float *dt_bias, const float *A,
+                           const uint16_t *B, const uint16_t *C, const float *D,
+                           const uint16_t *out, const ssu_shape_t *shape,
+                           const ssu_strides_t *st) {
+    if (!shape || !st) return fail(SSU_ERR_INVALID_ARG, "shape and strides must not be NULL");
+    const ssu_shape_t &s = *shape;
+    if (s.batch < 0) return fail(SSU_ERR_INVALID_ARG, "batch %lld < 0", (long long)s.batch);
+    if (s.nheads < 1 || s.headdim < 1 || s.dstate < 1 || s.ngroups < 1)
+        return fail(SSU_ERR_INVALID_ARG, "nheads, headdim, dstate and ngroups must be >= 1");
+    if (s.pool_size < 0) return fail(SSU_ERR_INVALID_ARG, "pool_size < 0");
+    if (s.nheads % s.ngroups != 0)
+        return fail(SSU_ERR_INVALID_ARG, "nheads %lld is not a multiple of ngroups %lld",
+                    (long long)s.nheads, (long long)s.ngroups);
+    if (s.index_dtype != SSU_INDEX_I32 && s.index_dtype != SSU_INDEX_I64)
+        return fail(SSU_ERR_INVALID_ARG, "index_dtype %d is neither I32 nor I64", s.index_dtype);
+    if (s.dstate != kDstate)
+        return fail(SSU_ERR_UNSUPPORTED, "dstate %lld: this build implements dstate 128",
+                    (long long)s.dstate);
+    if (s.headdim > (1 << 20) || s.nheads > (1 << 20))
+        return fail(SSU_ERR_UNSUPPORTED, "headdim and nheads are limited to 2^20");
+    if (s.batch == 0) return ok();  // nothing is read or written: strides are irrelevant
+
+    const int64_t *all[] = {st->state, st->x, st->out, st->dt, st->B, st->C,
+                            st->dt_bias, st->D, st->A};
+    const int lens[] = {4, 3, 3, 3, 3, 3, 2, 2, 3};
+    for (int i = 0; i < 9; ++i)
+        for (int j = 0; j < lens[i]; ++j)
+            if (all[i][j] < 0) return fail(SSU_ERR_INVALID_ARG, "negative stride");
+    if (st->idx < 0) return fail(SSU_ERR_INVALID_ARG, "negative index stride");
+    if (st->state[3] != 1) return fail(SSU_ERR_UNSUPPORTED, "state dstate-stride must be 1");
+    if (st->x[2] != 1) return fail(SSU_ERR_UNSUPPORTED, "x headdim-stride must be 1");
+    if (st->out[2] != 1) return fail(SSU_ERR_UNSUPPORTED, "out headdim-stride must be 1");
+    if (st->B[2] != 1 || st->C[2] != 1)
+        return fail(SSU_ERR_UNSUPPORTED, "B and C dstate-stride must be 1");
+    if (st->dt[2] != 0) return fail(SSU_ERR_UNSUPPORTED, "dt must be constant over headdim");
+    if (st->dt_bias[1] != 0 || st->D[1] != 0)
+        return fail(SSU_ERR_UNSUPPORTED, "dt_bias and D must be constant over headdim");
+    if (st->A[1] != 0 || st->A[2] != 0)
+        return fail(SSU_ERR_UNSUPPORTED, "A must be constant over headdim and dstate");
+    for (int j = 0; j < 3; ++j)
+        if (st->state[j] % 4 != 0)
+            return fail(SSU_ERR_MISALIGNED, "state stride %d (%lld) is not a multiple of 4 floats",
+                        j, (long long)st->state[j]);
+
+    if (!state_pool || !idx || !x || !dt || !dt_bias || !A || !B || !C || !D || !out)
+        return fail(SSU_ERR_INVALID_ARG, "a data pointer is NULL");
+    if (!aligned(state_pool, 16))
+        return fail(SSU_ERR_MISALIGNED, "state_pool is not 16-byte aligned");
+    if (!aligned(idx, s.index_dtype == SSU_INDEX_I64 ? 8 : 4))
+        return fail(SSU_ERR_MISALIGNED, "state_batch_indices is not aligned to its type");
+    if (!aligned(x, 2) || !aligned(dt, 2) || !aligned(B, 2) || !aligned(C, 2) || !aligned(out, 2))
+        return fail(SSU_ERR_MISALIGNED, "a bf16 operand is not 2-byte aligned");
+    if (!aligned(dt_bias, 4) || !aligned(A, 4) || !aligned(D, 4))
+        return fail(SSU_ERR_MISALIGNED, "an fp32 operand is not 4-byte aligned");
+    if (s.batch > INT_MAX / s.nheads)
+        return fail(SSU_ERR_UNSUPPORTED, "batch * nheads exceeds 2^31");
+    return ok();
+}
+
+}  // namespace ssu_host
+
+extern "C" {
+
+int32_t ssu_abi_version(void) { return SSU_ABI_VERSION; }
+
+const char *ssu_status_string(ssu_status_t status) {
+    switch (status) {
+        case SSU_OK: return "SSU_OK";
+        case SSU_ERR_INVALID_ARG: return "SSU_ERR_INVALID_ARG";
+        case SSU_ERR_UNSUPPORTED: return "SSU_ERR_UNSUPPORTED";
+        case SSU_ERR_MISALIGNED: return "SSU_ERR_MISALIGNED";
+        case SSU_ERR_CUDA: return "SSU_ERR_CUDA";
+        case SSU_ERR_INDEX_OOB: return "SSU_ERR_INDEX_OOB";
+        case SSU_ERR_TIMEOUT: return "SSU_ERR_TIMEOUT";
+    }
+    return "SSU_ERR_UNKNOWN";
+}
+
+const char *ssu_last_error(void) { return ssu_host::g_last_error.c_str(); }
+
+}  // extern "C"
