@@ -601,6 +601,177 @@ def run_calibrate(args) -> None:
                           "inplace_tbps": round(2 * nbytes / t_rmw / 1e6, 3)}), flush=True)
 
 
+# State-block copy workload (vLLM PR #48110, Test Plan / Microbenchmark): per request 24 fp32
+# temporal blocks of 2 MiB and 24 bf16 conv blocks of 80 KiB (49.875 MiB copied), distinct
+# source and destination blocks, at 1..128 requests.  Its GB200 figures (PR branch, GB/s of
+# read + write) are context: another machine.
+COPY_TEMPORAL = (32, 128, 128)     # fp32 elements per temporal block: 2 MiB
+COPY_CONV = (10240, 4)             # bf16 elements per conv block: 80 KiB
+COPY_LAYERS = 24
+COPY_REQS = (1, 4, 8, 16, 32, 64, 128)
+PAGE_COPY_GBS = {1: 479.4, 4: 1640.6, 8: 3050.0, 16: 4737.9, 32: 5900.6, 64: 5165.9,
+                 128: 5788.0}
+
+
+def copy_bytes_per_request() -> int:
+    t = 4 * int(np.prod(COPY_TEMPORAL))
+    c = 2 * int(np.prod(COPY_CONV))
+    return COPY_LAYERS * (t + c)
+
+
+class CopyWorkload:
+    """48 state tensors whose blocks cover `n_sets` disjoint (src, dst) sets of `reqs`."""
+
+    def __init__(self, reqs: int, dev, l2_bytes: int, seed: int = 0):
+        import torch
+        per_set = 2 * reqs * copy_bytes_per_request()
+        self.n_sets = max(3, -(-3 * l2_bytes // per_set))
+        blocks = 2 * reqs * self.n_sets
+        gen = torch.Generator(device=dev).manual_seed(seed)
+        self.tensors = []
+        for _ in range(COPY_LAYERS):
+            t = torch.empty((blocks,) + COPY_TEMPORAL, dtype=torch.float32, device=dev)
+            t.uniform_(-1, 1, generator=gen)
+            self.tensors.append(t)
+        for _ in range(COPY_LAYERS):
+            c = torch.empty((blocks,) + COPY_CONV, dtype=torch.bfloat16, device=dev)
+            c.uniform_(-1, 1, generator=gen)
+            self.tensors.append(c)
+        perm = torch.from_numpy(np.random.default_rng(seed).permutation(blocks).astype(np.int32))
+        perm = perm.view(self.n_sets, 2, reqs).to(dev)
+        self.src = [perm[k, 0].contiguous() for k in range(self.n_sets)]
+        self.dst = [perm[k, 1].contiguous() for k in range(self.n_sets)]
+        self.reqs = reqs
+
+    def call(self, handle, i: int, stream_ptr: int) -> None:
+        import selective_state_update_02_gb300 as ssu
+        k = i % self.n_sets
+        ssu.ssu_copy_blocks(handle, self.tensors, self.src[k], self.dst[k], stream_ptr)
+
+
+def run_copy(args) -> None:
+    """Block-copy throughput (GB/s of read + write) at 1..128 requests, one JSON line each;
+    with --sweep, every launch shape at 8, 32 and 128 requests instead."""
+    import torch
+
+    import selective_state_update_02_gb300 as ssu
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = ssu.ssu_create(0)
+    peaks = load_peaks()
+    shapes = [None]
+    reqs_list = COPY_REQS
+    if args.sweep:
+        reqs_list = (8, 32, 128)
+        shapes = ([(ssu.SSU_COPY_VEC, c, v, t) for c in (16, 32, 64) for v in (4, 8, 16)
+                   for t in (128, 256)] +
+                  [(ssu.SSU_COPY_BULK, c, st, 0) for c in (16, 32, 64) for st in (3, 4, 6)
+                   if 128 + st * c * 1024 <= 220 * 1024])
+    for reqs in reqs_list:
+        w = CopyWorkload(reqs, dev, l2)
+        moved = 2 * reqs * copy_bytes_per_request()
+        for shape in shapes:
+            if shape is None:
+                ssu.ssu_copy_set_launch(handle, ssu.SSU_COPY_AUTO)
+            else:
+                ssu.ssu_copy_set_launch(handle, *shape)
+            n = max(w.n_sets * 4, min(400, int(2e5 / (moved / 6e6))))
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    w.call(handle, i, stream.cuda_stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                cur = torch.cuda.current_stream().cuda_stream
+                for i in range(n):
+                    w.call(handle, i, cur)
+            g.replay()
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1) * 1000.0 / n)
+            gbs = moved / (best * 1e-6) / 1e9
+            rec = {"copy_reqs": reqs, "us_per_call": round(best, 3), "gbs": round(gbs, 1),
+                   "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4),
+                   "pages_gb200_gbs": PAGE_COPY_GBS.get(reqs), "calls": n, "sets": w.n_sets,
+                   "launch": list(shape) if shape else "table"}
+            print(json.dumps(rec), flush=True)
+            del g
+        del w
+        torch.cuda.empty_cache()
+    ssu.ssu_copy_set_launch(handle, ssu.SSU_COPY_AUTO)
+    assert ssu.ssu_get_error(handle) == (0, -1)
+    ssu.ssu_destroy(handle)
+
+
+def bytes_per_call_tokens(bs: int, T: int, intermediate: bool, H: int = NHEADS,
+                          P: int = HEADDIM, N: int = DSTATE, G: int = NGROUPS) -> int:
+    """Algorithmic bytes of one multi-token call: the state read and written once, T tokens of
+    inputs and outputs, and (optionally) T intermediate states written."""
+    state = 2 * bs * H * P * N * 4
+    per_token = bs * H * P * 2 * 2 + 2 * bs * G * N * 2 + bs * H * 2
+    inter = T * bs * H * P * N * 4 if intermediate else 0
+    return state + T * per_token + bs * 4 + 3 * H * 4 + inter
+
+
+def run_tokens(args) -> None:
+    """Multi-token step at batch 128 (cold-L2 rotation): µs per call and GB/s for T = 1..4,
+    with and without the intermediate-state output."""
+    import torch
+
+    import selective_state_update_02_gb300 as ssu
+    import workloads as wl
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = ssu.ssu_create(0)
+    bs, H = args.batch, NHEADS
+    w = Workload(bs, H, dev, seed=5, l2_bytes=l2)
+    rng = np.random.default_rng(9)
+    peaks = load_peaks()
+    for T in (1, 2, 3, 4):
+        x = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(
+            (w.n_sets, bs, T, H, HEADDIM), dtype=np.float32)).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        bc = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(
+            (w.n_sets, 2, bs, T, 1, DSTATE), dtype=np.float32)).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        dt = torch.from_numpy(wl.f32_to_bf16_bits(rng.uniform(
+            -4, 0, (w.n_sets, bs, T, H)).astype(np.float32)).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        out = torch.empty(bs, T, H, HEADDIM, dtype=torch.bfloat16, device=dev)
+        for with_inter in (False, True):
+            inter = (torch.empty(bs, T, H, HEADDIM, DSTATE, device=dev) if with_inter else None)
+
+            def call(i, stream_ptr, T=T, x=x, bc=bc, dt=dt, out=out, inter=inter):
+                k = i % w.n_sets
+                ssu.ssu_update_tokens(handle, w.pool, w.sets[k], x[k], dt[k], w.dt_bias, w.A,
+                                      bc[k, 0], bc[k, 1], w.D, out, inter, stream_ptr)
+
+            n = max(w.n_sets * 4, 400)
+            us = graph_time_us(lambda i: call(i, torch.cuda.current_stream().cuda_stream),
+                               w.n_sets, calls=n)
+            moved = bytes_per_call_tokens(bs, T, with_inter)
+            gbs = moved / (us * 1e-6) / 1e9
+            print(json.dumps({"tokens": T, "batch": bs, "intermediate": with_inter,
+                              "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
+                              "gbs": round(gbs, 1),
+                              "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4)}),
+                  flush=True)
+            del inter
+        del x, bc, dt, out
+        torch.cuda.empty_cache()
+    assert ssu.ssu_get_error(handle) == (0, -1)
+    ssu.ssu_destroy(handle)
+
+
 SWEEP_SHAPES = ([(1, r, w, 0) for r in (1, 2, 4, 8, 16) for w in (1, 2, 4, 8)] +
                 [(2, r, w, st) for r, w in ((4, 4), (8, 2), (8, 4), (16, 2), (16, 4), (8, 8),
                                             (4, 8), (2, 8))
@@ -656,6 +827,10 @@ def main() -> None:
     ap.add_argument("--launch", default="",
                     help="force a launch shape 'mode,rows_per_warp,warps_per_cta,stages' "
                          "(mode 1 = VEC, 2 = BULK) instead of the built-in table")
+    ap.add_argument("--tokens", action="store_true",
+                    help="multi-token step (T = 1..4) at --batch instead")
+    ap.add_argument("--copy", action="store_true",
+                    help="state-block copy throughput instead (with --sweep: its shapes)")
     ap.add_argument("--sweep", action="store_true", help="launch-shape sweep instead")
     ap.add_argument("--calibrate", action="store_true",
                     help="library copy / in-place rates at the call sizes instead")
@@ -667,7 +842,11 @@ def main() -> None:
     args = ap.parse_args()
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
-    if args.calibrate:
+    if args.tokens:
+        run_tokens(args)
+    elif args.copy:
+        run_copy(args)
+    elif args.calibrate:
         run_calibrate(args)
     elif args.sweep:
         run_sweep(args)

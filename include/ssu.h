@@ -175,6 +175,95 @@ ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch);
 ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
                             ssu_launch_t *launch);
 
+/* ---------------------------------------------------------------------------------------
+ * Multi-token step: T consecutive tokens of every request in one call, as multi-token
+ * speculation verifies them (vLLM PR #48110, Test Plan: speculative decoding with two draft
+ * tokens per step).  Token t applies the decode step above to the state left by token t - 1:
+ *
+ *   for t = 0 .. T-1:
+ *     dtv = softplus(dt[b,t,h] + dt_bias[h]);   dA = exp(dtv * A[h])
+ *     S[p,n] = S[p,n] * dA + (dtv * x[b,t,h,p]) * B[b,t,g,n]
+ *     out[b,t,h,p] = bf16_rne( sum_n S[p,n] * C[b,t,g,n] + D[h] * x[b,t,h,p] )
+ *     if intermediate: intermediate[b,t,h,p,n] = S[p,n]        (fp32)
+ *   state_pool[s,h] = S
+ *
+ * The state is read once and written once per call, whatever T; with T = 1 and no
+ * intermediate buffer the result is bit-identical to ssu_update.
+ */
+
+/* Token strides (elements) of the per-token operands, and the optional intermediate buffer. */
+typedef struct {
+    int64_t x, out, dt, B, C;  /* stride of the token index t in x, out, dt, B and C; the
+                                  other strides come from ssu_strides_t */
+    int64_t intermediate[5];   /* [bs, T, H, P, N]: N-stride 1, the others multiples of 4 */
+} ssu_token_strides_t;
+
+#define SSU_MAX_TOKENS 64
+
+/*
+ * T consecutive decode steps (1 <= T <= SSU_MAX_TOKENS).  Pointers, shape and ssu_strides_t as
+ * for ssu_update (describing token 0), plus `tokens` = T, the token strides, and
+ * `intermediate` (device fp32, 16-byte aligned, or NULL for none).  Same error behaviour as
+ * ssu_update; enqueued on `stream`; allocates and synchronises nothing.
+ */
+ssu_status_t ssu_update_tokens(ssu_handle_t handle, float *state_pool,
+                               const void *state_batch_indices, const uint16_t *x,
+                               const uint16_t *dt, const float *dt_bias, const float *A,
+                               const uint16_t *B, const uint16_t *C, const float *D,
+                               uint16_t *out, float *intermediate, const ssu_shape_t *shape,
+                               const ssu_strides_t *strides, int64_t tokens,
+                               const ssu_token_strides_t *token_strides, ssu_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * State-block copy (vLLM PR #48110, Purpose and Test Plan / Microbenchmark): under prefix
+ * caching and multi-token speculation a request's recurrent states are copied from one cache
+ * block to another, for every state tensor of the model (one temporal fp32 state and one conv
+ * state per hybrid layer).  One call copies, for every request i and every described tensor,
+ * block src_idx[i] to block dst_idx[i] of that tensor.  Bytes are copied verbatim.
+ */
+
+/* One state tensor viewed as blocks: block k is block_bytes bytes at base + k * stride. */
+typedef struct {
+    void *base;                 /* device pointer, 16-byte aligned */
+    int64_t block_bytes;        /* bytes copied per block: > 0, a multiple of 16 */
+    int64_t block_stride_bytes; /* distance between blocks: a multiple of 16, >= block_bytes */
+    int64_t num_blocks;         /* valid block ids are [0, num_blocks) */
+} ssu_block_tensor_t;
+
+#define SSU_COPY_MAX_TENSORS 64
+
+typedef enum {
+    SSU_COPY_AUTO = 0,  /* built-in choice */
+    SSU_COPY_VEC = 1,   /* 16-byte vector loads and stores through registers */
+    SSU_COPY_BULK = 2   /* bulk asynchronous copies (TMA engine) through shared memory */
+} ssu_copy_mode_t;
+
+typedef struct {
+    int32_t mode;        /* ssu_copy_mode_t */
+    int32_t chunk_kib;   /* bytes per work item, KiB: 4, 8, 16, 32 or 64 */
+    int32_t stages;      /* BULK: shared-memory ring depth, 2..8; VEC: 16-byte vectors per thread
+                            per pass, 1..16 */
+    int32_t threads;     /* VEC: threads per CTA, 32..256 (multiple of 32); BULK: ignored */
+} ssu_copy_launch_t;
+
+/*
+ * Copy block src_idx[i] -> block dst_idx[i] of each of the `num_tensors` tensors (host array,
+ * at most SSU_COPY_MAX_TENSORS), for i in [0, n).  src_idx and dst_idx are device int32 or
+ * int64 arrays (index_dtype) of n entries.  A request whose src or dst id is out of a tensor's
+ * range is skipped for every tensor and counted (ssu_get_error).  Preconditions (not checked):
+ * the dst ids are distinct and no dst id equals a src id of the same call (the copies run
+ * concurrently).  Enqueued on `stream`; allocates and synchronises nothing.  Errors: NULL or
+ * misaligned pointers, sizes or strides that are not multiples of 16 -> SSU_ERR_MISALIGNED /
+ * SSU_ERR_INVALID_ARG before anything is enqueued.
+ */
+ssu_status_t ssu_copy_blocks(ssu_handle_t handle, const ssu_block_tensor_t *tensors,
+                             int32_t num_tensors, const void *src_idx, const void *dst_idx,
+                             int64_t n, int32_t index_dtype, ssu_stream_t stream);
+
+/* Force a launch shape for later ssu_copy_blocks calls on this handle (NULL or mode AUTO
+ * restores the built-in choice).  All shapes copy the same bytes. */
+ssu_status_t ssu_copy_set_launch(ssu_handle_t handle, const ssu_copy_launch_t *launch);
+
 /*
  * Allocation-free variant of ssu_update.  No counterpart exists in the paper: it serves
  * callers that cannot call cudaMalloc, such as code running under an allocator that must not

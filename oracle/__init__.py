@@ -137,3 +137,43 @@ def ssu_step(pool, idx, x, dt, dt_bias, A, B, C, D, ngroups: int = 1):
     pool64 = np.array(pool, dtype=np.float64, order="C", copy=True)
     y, skipped = ssu_step_inplace(pool64, idx, x, dt, dt_bias, A, B, C, D, ngroups)
     return pool64, y, skipped
+
+
+def copy_blocks(tensors, src, dst):
+    """State-block copy, written out plainly (vLLM PR #48110, Purpose): for every request i
+    and every tensor (an array whose first axis indexes blocks), block dst[i] receives the
+    bytes of block src[i].  Returns new arrays; a request whose ids fall outside any tensor's
+    range is skipped for every tensor.  Returns (new_tensors, skipped)."""
+    out = [np.array(t, copy=True) for t in tensors]
+    skipped = 0
+    for s_, d_ in zip(np.asarray(src).tolist(), np.asarray(dst).tolist()):
+        if not all(0 <= s_ < len(t) and 0 <= d_ < len(t) for t in tensors):
+            skipped += 1
+            continue
+        for t, o in zip(tensors, out):
+            o[d_] = t[s_]
+    return out, skipped
+
+
+def ssu_tokens(pool, idx, x, dt, dt_bias, A, B, C, D, ngroups: int = 1):
+    """T consecutive decode steps: the single step above applied to tokens t = 0 .. T-1 in
+    order, each starting from the state the previous token left (the multi-token verification
+    of speculative decoding, vLLM PR #48110, Test Plan).  ``x`` is ``[bs, T, H, P]``, ``dt``
+    ``[bs, T, H]``, ``B``/``C`` ``[bs, T, G, N]`` (bf16 patterns).  Returns
+    ``(new_pool64, y64 [bs, T, H, P], intermediate64 [bs, T, H, P, N], skipped)``;
+    intermediate[b, t] is request b's state after token t (NaN for skipped requests)."""
+    pool64 = np.array(pool, dtype=np.float64, order="C", copy=True)
+    x = np.asarray(x)
+    bs, T, H, P = x.shape
+    N = pool64.shape[3]
+    idx = np.asarray(idx, dtype=np.int64)
+    ok = (idx >= 0) & (idx < pool64.shape[0])
+    y = np.empty((bs, T, H, P))
+    inter = np.full((bs, T, H, P, N), np.nan)
+    skipped = 0
+    for t in range(T):
+        y[:, t], skipped = ssu_step_inplace(pool64, idx, x[:, t], np.asarray(dt)[:, t], dt_bias,
+                                            A, np.asarray(B)[:, t], np.asarray(C)[:, t], D,
+                                            ngroups)
+        inter[ok, t] = pool64[idx[ok]]
+    return pool64, y, inter, skipped

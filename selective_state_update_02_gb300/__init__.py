@@ -58,6 +58,30 @@ class ssu_launch_t(ctypes.Structure):
                 ("warps_per_cta", ctypes.c_int32), ("stages", ctypes.c_int32)]
 
 
+class ssu_token_strides_t(ctypes.Structure):
+    _fields_ = [("x", _i64), ("out", _i64), ("dt", _i64), ("B", _i64), ("C", _i64),
+                ("intermediate", _i64 * 5)]
+
+
+SSU_MAX_TOKENS = 64
+
+
+class ssu_block_tensor_t(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("block_bytes", _i64),
+                ("block_stride_bytes", _i64), ("num_blocks", _i64)]
+
+
+class ssu_copy_launch_t(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("chunk_kib", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("threads", ctypes.c_int32)]
+
+
+SSU_COPY_AUTO = 0
+SSU_COPY_VEC = 1
+SSU_COPY_BULK = 2
+SSU_COPY_MAX_TENSORS = 64
+
+
 class SsuError(RuntimeError):
     def __init__(self, status: int, where: str, message: str):
         self.status = status
@@ -81,6 +105,13 @@ _EXPORTS = {
     "ssu_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_launch_t)]),
     "ssu_get_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_shape_t),
                                       ctypes.POINTER(ssu_launch_t)]),
+    "ssu_update_tokens": (ctypes.c_int, [_vp] * 12 + [ctypes.POINTER(ssu_shape_t),
+                                                      ctypes.POINTER(ssu_strides_t),
+                                                      ctypes.c_int64,
+                                                      ctypes.POINTER(ssu_token_strides_t), _vp]),
+    "ssu_copy_blocks": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_block_tensor_t), ctypes.c_int32,
+                                       _vp, _vp, ctypes.c_int64, ctypes.c_int32, _vp]),
+    "ssu_copy_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_copy_launch_t)]),
     "ssu_update_static": (ctypes.c_int, [_vp] * 10 + [ctypes.POINTER(ssu_shape_t),
                                                       ctypes.POINTER(ssu_strides_t), _vp, _vp]),
 }
@@ -288,6 +319,75 @@ def ssu_get_launch(handle: int, shape: ssu_shape_t) -> tuple[int, int, int, int]
     return cfg.mode, cfg.rows_per_warp, cfg.warps_per_cta, cfg.stages
 
 
+def ssu_update_tokens(handle: int, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
+                      out, intermediate=None, stream=None) -> None:
+    """T consecutive decode steps per request.  ``x`` and ``out`` are ``[bs, T, H, P]``;
+    ``dt`` is ``[bs, T, H]`` (or ``[bs, T, H, P]`` with stride 0 over P); ``B`` and ``C`` are
+    ``[bs, T, G, N]``; ``intermediate`` (optional, fp32 ``[bs, T, H, P, N]``) receives the
+    state after every token.  Per-head operands as for ``ssu_update``."""
+    for name, t, nd in (("x", x, 4), ("out", out, 4), ("B", B, 4), ("C", C, 4)):
+        if not isinstance(t, torch.Tensor) or t.dim() != nd:
+            raise ValueError(f"{name} must be a {nd}-D tensor with a token dimension")
+    if dt.dim() not in (3, 4):
+        raise ValueError("dt must be [bs, T, H] or [bs, T, H, P]")
+    T = x.shape[1]
+    for name, t in (("out", out), ("dt", dt), ("B", B), ("C", C)):
+        if t.shape[1] != T:
+            raise ValueError(f"{name} must have {T} tokens")
+    shape, strides = describe(state_pool, state_batch_indices, x[:, 0], dt[:, 0], dt_bias, A,
+                              B[:, 0], C[:, 0], D, out[:, 0])
+    ts = ssu_token_strides_t()
+    ts.x, ts.out, ts.dt, ts.B, ts.C = (x.stride(1), out.stride(1), dt.stride(1), B.stride(1),
+                                       C.stride(1))
+    if intermediate is not None:
+        _expect(intermediate, "intermediate", torch.float32, (5,))
+        if tuple(intermediate.shape) != (x.shape[0], T, x.shape[2], x.shape[3],
+                                         state_pool.shape[3]):
+            raise ValueError("intermediate must be [bs, T, H, P, N]")
+        ts.intermediate[:] = list(intermediate.stride())
+    ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out,
+                               intermediate)]
+    _check(lib().ssu_update_tokens(handle, *ptrs, ctypes.byref(shape), ctypes.byref(strides), T,
+                                   ctypes.byref(ts), _stream_ptr(stream)), "ssu_update_tokens")
+
+
+def describe_blocks(tensors) -> tuple[ctypes.Array, int]:
+    """ABI descriptors for state tensors laid out as ``[num_blocks, ...]``: block k is the
+    slice ``t[k]``, which must be contiguous (its bytes are copied verbatim)."""
+    arr = (ssu_block_tensor_t * len(tensors))()
+    for i, t in enumerate(tensors):
+        if not isinstance(t, torch.Tensor) or t.dim() < 1:
+            raise TypeError("each state tensor must be a torch.Tensor of >= 1 dims")
+        if t.dim() > 1 and not t[0].is_contiguous():
+            raise ValueError("each block (t[k]) must be contiguous")
+        item = t.element_size()
+        block = item * (t[0].numel() if t.dim() > 1 else 1)
+        arr[i] = ssu_block_tensor_t(t.data_ptr(), block, t.stride(0) * item, t.shape[0])
+    return arr, len(tensors)
+
+
+def ssu_copy_blocks(handle: int, tensors, src_idx, dst_idx, stream=None) -> None:
+    """Copy block src_idx[i] -> dst_idx[i] of every tensor in ``tensors`` (each
+    ``[num_blocks, ...]``), for every request i.  Enqueued on ``stream``."""
+    if src_idx.dtype != dst_idx.dtype or src_idx.dtype not in (torch.int32, torch.int64):
+        raise TypeError("src_idx and dst_idx must both be int32 or both int64")
+    if src_idx.dim() != 1 or src_idx.shape != dst_idx.shape:
+        raise ValueError("src_idx and dst_idx must be 1-D of the same length")
+    if not (src_idx.is_contiguous() and dst_idx.is_contiguous()):
+        raise ValueError("src_idx and dst_idx must be contiguous")
+    arr, count = describe_blocks(tensors)
+    dtype = SSU_INDEX_I64 if src_idx.dtype == torch.int64 else SSU_INDEX_I32
+    _check(lib().ssu_copy_blocks(handle, arr, count, src_idx.data_ptr(), dst_idx.data_ptr(),
+                                 src_idx.shape[0], dtype, _stream_ptr(stream)),
+           "ssu_copy_blocks")
+
+
+def ssu_copy_set_launch(handle: int, mode: int = SSU_COPY_AUTO, chunk_kib: int = 32,
+                        stages: int = 8, threads: int = 256) -> None:
+    cfg = ssu_copy_launch_t(mode, chunk_kib, stages, threads)
+    _check(lib().ssu_copy_set_launch(handle, ctypes.byref(cfg)), "ssu_copy_set_launch")
+
+
 class SelectiveStateUpdate:
     """Owns one handle; ``__call__`` is ``ssu_update`` on it."""
 
@@ -302,6 +402,15 @@ class SelectiveStateUpdate:
         ssu_update(self.handle, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
                    out, stream)
         return out
+
+    def tokens(self, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out,
+               intermediate=None, stream=None):
+        ssu_update_tokens(self.handle, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C,
+                          D, out, intermediate, stream)
+        return out
+
+    def copy_blocks(self, tensors, src_idx, dst_idx, stream=None):
+        ssu_copy_blocks(self.handle, tensors, src_idx, dst_idx, stream)
 
     def get_error(self, stream=None):
         return ssu_get_error(self.handle, stream)

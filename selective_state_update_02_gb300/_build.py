@@ -11,7 +11,7 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 CSRC = PKG / "csrc"
-SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_host.cpp"]
+SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_tokens.cu", CSRC / "ssu_copy.cu", CSRC / "ssu_host.cpp"]
 HEADERS = [ROOT / "include" / "ssu.h", CSRC / "ssu_device.cuh", CSRC / "ssu_host.h"]
 OBJDIR = PKG / "_build"
 LIB = PKG / "libssu.so"

@@ -417,6 +417,7 @@ ssu_status_t ssu_create(ssu_handle_t *out, int32_t device) {
         for (int i64 = 0; e == cudaSuccess && i64 < 2; ++i64)
             e = cudaFuncSetAttribute(reinterpret_cast<const void *>(bulk_kernel(rpw, i64 != 0)),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin);
+    if (e == cudaSuccess) e = ssu_host::copy_prepare(h->smem_optin);
     if (e == cudaSuccess) e = cudaMalloc(&h->err, 4 * sizeof(unsigned));
     const unsigned init[4] = {0u, 0xffffffffu, 0u, 0u};
     if (e == cudaSuccess) e = cudaMemcpy(h->err, init, sizeof(init), cudaMemcpyHostToDevice);

@@ -1,0 +1,349 @@
+// State-block copy for GB300 (sm_103a): block src_idx[i] -> block dst_idx[i] of every state
+// tensor (vLLM PR #48110, Purpose and Test Plan / Microbenchmark describe the operation: the
+// temporal and conv states of each hybrid layer are copied between cache blocks under prefix
+// caching and multi-token speculation).  Pure data movement, bound by HBM bandwidth.
+//
+// Work decomposition.  Every (tensor, request) block is cut into chunks of `chunk_bytes`;
+// chunks of tensor t occupy a contiguous range of a global chunk index (tensor-major, then
+// request, then chunk), so the whole call is one flat list that persistent CTAs stride through.
+//
+// VEC: each thread moves `vectors` 16-byte words per pass, all loads issued before the stores.
+// BULK: one thread per CTA drives the TMA engine: 1-D `cp.async.bulk` loads of whole chunks
+// into a ring of shared-memory stages (completion on the stage's mbarrier), each followed by a
+// 1-D bulk store of the stage to its destination; a stage is reused once the store issued from
+// it has been read out (`cp.async.bulk.wait_group.read`).  Every mbarrier wait is bounded.
+
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "ssu.h"
+#include "ssu_device.cuh"
+#include "ssu_host.h"
+
+using ssu_host::aligned;
+using ssu_host::DeviceGuard;
+using ssu_host::fail;
+using ssu_host::ok;
+
+namespace {
+
+struct CopyTensor {
+    char *base;
+    long long block_bytes;
+    long long stride;
+    long long num_blocks;
+    long long chunks;       // chunks per block
+    long long chunk_begin;  // first global chunk index of this tensor
+};
+
+struct CopyParams {
+    CopyTensor t[SSU_COPY_MAX_TENSORS];
+    const void *src;
+    const void *dst;
+    long long n;
+    long long total_chunks;
+    long long chunk_bytes;
+    int num_tensors;
+    int idx64;
+    unsigned *err;  // [0] skipped requests, [1] smallest skipped request, [2] timeouts
+};
+
+struct ChunkRef {
+    const char *src;
+    char *dst;
+    unsigned bytes;
+    bool valid;
+};
+
+__device__ __forceinline__ long long load_id(const void *ids, int idx64, long long i) {
+    return idx64 ? __ldg(static_cast<const long long *>(ids) + i)
+                 : static_cast<long long>(__ldg(static_cast<const int *>(ids) + i));
+}
+
+// Locates global chunk c: its tensor, request, source and destination.
+__device__ __forceinline__ ChunkRef locate_chunk(const CopyParams &p, long long c) {
+    int t = 0;
+    while (t + 1 < p.num_tensors && c >= p.t[t + 1].chunk_begin) ++t;
+    const CopyTensor &T = p.t[t];
+    const long long local = c - T.chunk_begin;
+    const long long i = local / T.chunks;
+    const long long k = local - i * T.chunks;
+    const long long s = load_id(p.src, p.idx64, i);
+    const long long d = load_id(p.dst, p.idx64, i);
+    ChunkRef r;
+    // A request is skipped for every tensor if any of its ids is out of any tensor's range.
+    bool valid = true;
+    for (int u = 0; u < p.num_tensors; ++u)
+        valid = valid && s >= 0 && d >= 0 && s < p.t[u].num_blocks && d < p.t[u].num_blocks;
+    r.valid = valid;
+    const long long off = k * p.chunk_bytes;
+    const long long rest = T.block_bytes - off;
+    r.bytes = static_cast<unsigned>(rest < p.chunk_bytes ? rest : p.chunk_bytes);
+    r.src = T.base + s * T.stride + off;
+    r.dst = T.base + d * T.stride + off;
+    if (!valid && t == 0 && k == 0 && (threadIdx.x == 0)) {
+        atomicAdd(&p.err[0], 1u);
+        atomicMin(&p.err[1], static_cast<unsigned>(i));
+    }
+    return r;
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) copy_vec_kernel(const __grid_constant__ CopyParams p) {
+    const long long pass = static_cast<long long>(blockDim.x) * 16 * V;
+    for (long long c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
+        const ChunkRef r = locate_chunk(p, c);
+        if (!r.valid) continue;
+        for (long long base = 0; base < r.bytes; base += pass) {
+            uint4 v[V];
+#pragma unroll
+            for (int u = 0; u < V; ++u) {
+                const long long o = base + (static_cast<long long>(u) * blockDim.x + threadIdx.x) * 16;
+                if (o < r.bytes) v[u] = __ldcs(reinterpret_cast<const uint4 *>(r.src + o));
+            }
+#pragma unroll
+            for (int u = 0; u < V; ++u) {
+                const long long o = base + (static_cast<long long>(u) * blockDim.x + threadIdx.x) * 16;
+                if (o < r.bytes) __stcs(reinterpret_cast<uint4 *>(r.dst + o), v[u]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N committed bulk-store groups may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// One thread per CTA (threadIdx.x == 0) drives the ring; `stages` is at most kMaxStages.
+// Loads run L = stages - 2 chunks ahead of the stores, so a stage is refilled once the store
+// issued two iterations earlier has been read out (wait_group.read 1).
+__global__ void __launch_bounds__(32) copy_bulk_kernel(const __grid_constant__ CopyParams p,
+                                                       int stages) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    if (threadIdx.x != 0) return;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
+    unsigned char *buf = smem_raw + 128;
+    const unsigned chunk = static_cast<unsigned>(p.chunk_bytes);
+    const long long G = gridDim.x;
+    const long long n_my = (p.total_chunks - blockIdx.x + G - 1) / G;
+    const int L = stages - 2;
+    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+
+    unsigned valid_bits = 0;  // bit s: the chunk loaded into stage s is to be stored
+    ChunkRef ref[kMaxStages];
+    bool failed = false;
+    long long issued = 0;
+    for (long long j = 0; j < n_my + L; ++j) {
+        if (j < n_my) {  // load chunk j into stage j % stages
+            const int st = static_cast<int>(j % stages);
+            if (j >= stages) bulk_wait_read<1>();
+            const ChunkRef r = locate_chunk(p, blockIdx.x + j * G);
+            ref[st] = r;
+            if (r.valid) {
+                valid_bits |= 1u << st;
+                mbar_arrive_expect_tx(&full[st], r.bytes);
+                bulk_load(buf + static_cast<size_t>(st) * chunk, r.src, r.bytes, &full[st]);
+            } else {
+                valid_bits &= ~(1u << st);
+                mbar_arrive(&full[st]);
+            }
+            issued = j + 1;
+        }
+        const long long m = j - L;  // store chunk m
+        if (m >= 0 && m < n_my) {
+            const int st = static_cast<int>(m % stages);
+            if (!mbar_wait(&full[st], static_cast<unsigned>((m / stages) & 1))) {
+                failed = true;
+                break;
+            }
+            if (valid_bits & (1u << st))
+                bulk_store(ref[st].dst, buf + static_cast<size_t>(st) * chunk, ref[st].bytes);
+            bulk_commit();  // one group per iteration (empty for a skipped chunk), so the
+                            // wait_group.read count above always names the right store
+        }
+    }
+    bulk_wait_all();
+    if (failed) {
+        atomicAdd(&p.err[2], 1u);
+        for (long long j = issued > stages ? issued - stages : 0; j < issued; ++j)
+            mbar_wait(&full[j % stages], static_cast<unsigned>((j / stages) & 1));
+    }
+}
+
+cudaError_t launch_copy_vec(const CopyParams &p, int vectors, int threads, unsigned grid,
+                            cudaStream_t st) {
+    switch (vectors) {
+        case 1: copy_vec_kernel<1><<<grid, threads, 0, st>>>(p); break;
+        case 2: copy_vec_kernel<2><<<grid, threads, 0, st>>>(p); break;
+        case 4: copy_vec_kernel<4><<<grid, threads, 0, st>>>(p); break;
+        case 8: copy_vec_kernel<8><<<grid, threads, 0, st>>>(p); break;
+        case 16: copy_vec_kernel<16><<<grid, threads, 0, st>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+using VecCopyKernel = void (*)(CopyParams);
+
+VecCopyKernel vec_copy_kernel(int vectors) {
+    switch (vectors) {
+        case 1: return copy_vec_kernel<1>;
+        case 2: return copy_vec_kernel<2>;
+        case 4: return copy_vec_kernel<4>;
+        case 8: return copy_vec_kernel<8>;
+        case 16: return copy_vec_kernel<16>;
+        default: return nullptr;
+    }
+}
+
+bool copy_launch_ok(const ssu_copy_launch_t &l) {
+    const int c = l.chunk_kib;
+    if (c != 4 && c != 8 && c != 16 && c != 32 && c != 64) return false;
+    if (l.mode == SSU_COPY_VEC)
+        return vec_copy_kernel(l.stages) != nullptr && l.threads >= 32 && l.threads <= 256 &&
+               l.threads % 32 == 0;
+    if (l.mode == SSU_COPY_BULK) return l.stages >= 3 && l.stages <= kMaxStages;
+    return false;
+}
+
+// Built-in choice, from the cold-L2 sweep on GB300 (bench.py --copy --sweep): 128-thread VEC
+// CTAs; calls under 1 GiB use 16 KiB chunks with 8 x 16 bytes per thread per pass, larger
+// calls 64 KiB chunks with 16 x 16 bytes (one pass per chunk either way).
+ssu_copy_launch_t copy_table(long long total_bytes) {
+    if (total_bytes >= (1LL << 30)) return ssu_copy_launch_t{SSU_COPY_VEC, 64, 16, 128};
+    return ssu_copy_launch_t{SSU_COPY_VEC, 16, 8, 128};
+}
+
+}  // namespace
+
+namespace ssu_host {
+
+cudaError_t copy_prepare(int smem_optin) {
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(copy_bulk_kernel),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+}
+
+}  // namespace ssu_host
+
+extern "C" {
+
+ssu_status_t ssu_copy_set_launch(ssu_handle_t handle, const ssu_copy_launch_t *launch) {
+    if (!handle) return fail(SSU_ERR_INVALID_ARG, "NULL handle");
+    if (!launch || launch->mode == SSU_COPY_AUTO) {
+        handle->has_copy_override = false;
+        return ok();
+    }
+    if (!copy_launch_ok(*launch))
+        return fail(SSU_ERR_UNSUPPORTED, "copy launch mode=%d chunk_kib=%d stages=%d threads=%d",
+                    launch->mode, launch->chunk_kib, launch->stages, launch->threads);
+    if (launch->mode == SSU_COPY_BULK &&
+        128 + launch->stages * launch->chunk_kib * 1024 > handle->smem_optin)
+        return fail(SSU_ERR_UNSUPPORTED, "BULK copy stages x chunk exceed shared memory");
+    handle->copy_override = *launch;
+    handle->has_copy_override = true;
+    return ok();
+}
+
+ssu_status_t ssu_copy_blocks(ssu_handle_t handle, const ssu_block_tensor_t *tensors,
+                             int32_t num_tensors, const void *src_idx, const void *dst_idx,
+                             int64_t n, int32_t index_dtype, ssu_stream_t stream) {
+    if (!handle) return fail(SSU_ERR_INVALID_ARG, "NULL handle");
+    if (n < 0) return fail(SSU_ERR_INVALID_ARG, "n < 0");
+    if (num_tensors < 1 || num_tensors > SSU_COPY_MAX_TENSORS)
+        return fail(SSU_ERR_INVALID_ARG, "num_tensors %d outside 1..%d", num_tensors,
+                    SSU_COPY_MAX_TENSORS);
+    if (!tensors) return fail(SSU_ERR_INVALID_ARG, "tensors is NULL");
+    if (index_dtype != SSU_INDEX_I32 && index_dtype != SSU_INDEX_I64)
+        return fail(SSU_ERR_INVALID_ARG, "index_dtype %d is neither I32 nor I64", index_dtype);
+    for (int t = 0; t < num_tensors; ++t) {
+        const ssu_block_tensor_t &T = tensors[t];
+        if (!T.base) return fail(SSU_ERR_INVALID_ARG, "tensor %d: NULL base", t);
+        if (T.block_bytes <= 0 || T.num_blocks < 0 || T.block_stride_bytes < T.block_bytes)
+            return fail(SSU_ERR_INVALID_ARG, "tensor %d: bad block size/stride/count", t);
+        if (!aligned(T.base, 16) || T.block_bytes % 16 || T.block_stride_bytes % 16)
+            return fail(SSU_ERR_MISALIGNED,
+                        "tensor %d: base, block size and stride must be multiples of 16 bytes",
+                        t);
+    }
+    if (n == 0) return ok();
+    if (!src_idx || !dst_idx) return fail(SSU_ERR_INVALID_ARG, "src_idx or dst_idx is NULL");
+    const unsigned isz = index_dtype == SSU_INDEX_I64 ? 8 : 4;
+    if (!aligned(src_idx, isz) || !aligned(dst_idx, isz))
+        return fail(SSU_ERR_MISALIGNED, "index arrays are not aligned to their type");
+    if (n > UINT_MAX - 1) return fail(SSU_ERR_UNSUPPORTED, "n exceeds 2^32 - 2");
+
+    long long total_bytes = 0;
+    for (int t = 0; t < num_tensors; ++t) total_bytes += n * tensors[t].block_bytes;
+    const ssu_copy_launch_t l =
+        handle->has_copy_override ? handle->copy_override : copy_table(total_bytes);
+    CopyParams p{};
+    p.chunk_bytes = static_cast<long long>(l.chunk_kib) * 1024;
+    long long chunks = 0;
+    for (int t = 0; t < num_tensors; ++t) {
+        CopyTensor &T = p.t[t];
+        T.base = static_cast<char *>(tensors[t].base);
+        T.block_bytes = tensors[t].block_bytes;
+        T.stride = tensors[t].block_stride_bytes;
+        T.num_blocks = tensors[t].num_blocks;
+        T.chunks = (T.block_bytes + p.chunk_bytes - 1) / p.chunk_bytes;
+        T.chunk_begin = chunks;
+        chunks += n * T.chunks;
+    }
+    p.src = src_idx;
+    p.dst = dst_idx;
+    p.n = n;
+    p.total_chunks = chunks;
+    p.num_tensors = num_tensors;
+    p.idx64 = index_dtype == SSU_INDEX_I64;
+    p.err = handle->err;
+
+    DeviceGuard guard(handle->device);
+    if (guard.err != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    int per_sm = 0;
+    if (l.mode == SSU_COPY_BULK) {
+        const int smem = 128 + l.stages * l.chunk_kib * 1024;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, copy_bulk_kernel, 32, smem);
+        if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
+        if (e == cudaSuccess) {
+            const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
+            const unsigned grid = static_cast<unsigned>(chunks < slots ? chunks : slots);
+            copy_bulk_kernel<<<grid, 32, smem, cs>>>(p, l.stages);
+            e = cudaGetLastError();
+        }
+    } else {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vec_copy_kernel(l.stages),
+                                                          l.threads, 0);
+        if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
+        if (e == cudaSuccess) {
+            const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
+            const unsigned grid = static_cast<unsigned>(chunks < slots ? chunks : slots);
+            e = launch_copy_vec(p, l.stages, l.threads, grid, cs);
+        }
+    }
+    if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "copy launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+}  // extern "C"

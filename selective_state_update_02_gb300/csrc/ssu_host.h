@@ -22,6 +22,10 @@ ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint1
                            const uint16_t *out, const ssu_shape_t *shape,
                            const ssu_strides_t *st);
 
+// Lets the BULK block-copy kernel use up to `smem_optin` bytes of dynamic shared memory
+// (called once per handle by ssu_create, on the handle's device).
+cudaError_t copy_prepare(int smem_optin);
+
 // Restores the caller's current device on scope exit.
 struct DeviceGuard {
     int prev = -1;
@@ -48,4 +52,6 @@ struct ssu_handle_s {
     unsigned *err = nullptr;  // device: [0] skipped, [1] smallest skipped request, [2] timeouts
     bool has_override = false;
     ssu_launch_t override_launch{};
+    bool has_copy_override = false;
+    ssu_copy_launch_t copy_override{};
 };

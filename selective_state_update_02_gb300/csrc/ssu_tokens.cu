@@ -1,0 +1,237 @@
+// Multi-token decode step for GB300 (sm_103a): T consecutive tokens of every request in one
+// call (the verification step of multi-token speculation, vLLM PR #48110, Test Plan).  Token t
+// applies the single-token update to the state token t - 1 left; the state is loaded once,
+// kept in registers across the T tokens, and stored once.  The element mapping, update order
+// and readout tree are those of the single-token VEC kernel (ssu_device.cuh), so T = 1
+// reproduces ssu_update bit for bit.  Each warp prefetches token t + 1's inputs (dt, its 4
+// columns of B and C, one x row per lane) while it updates token t.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "ssu.h"
+#include "ssu_device.cuh"
+#include "ssu_host.h"
+
+using ssu_host::aligned;
+using ssu_host::DeviceGuard;
+using ssu_host::fail;
+using ssu_host::ok;
+using ssu_host::validate_impl;
+
+namespace {
+
+struct TokenParams {
+    SsuParams p;
+    float *inter;                      // optional intermediate states, may be null
+    long long x_t, out_t, dt_t, B_t, C_t;
+    long long in_b, in_t, in_h, in_p;  // intermediate strides; dstate stride is 1
+    int tokens;
+};
+
+// One token's inputs for one warp: lane r < RPW holds x of row r.
+struct TokenIn {
+    float dt;
+    float bb[4], cc[4];
+    float x;
+};
+
+template <int RPW>
+__device__ __forceinline__ TokenIn load_token(const TokenParams &q, long long b, int h, int g,
+                                              int row0, int t, int lane) {
+    const SsuParams &p = q.p;
+    TokenIn in;
+    in.dt = __bfloat162float(p.dt[b * p.dt_b + t * q.dt_t + h * p.dt_h]);
+    const __nv_bfloat16 *Bp = p.B + b * p.B_b + t * q.B_t + g * p.B_g + lane * 4;
+    const __nv_bfloat16 *Cp = p.C + b * p.C_b + t * q.C_t + g * p.C_g + lane * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        in.bb[j] = __bfloat162float(Bp[j]);
+        in.cc[j] = __bfloat162float(Cp[j]);
+    }
+    in.x = (lane < RPW && row0 + lane < p.headdim)
+               ? __bfloat162float(p.x[b * p.x_b + t * q.x_t + h * p.x_h + row0 + lane])
+               : 0.f;
+    return in;
+}
+
+template <int RPW, bool kIdx64>
+__global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
+    ssu_tokens_kernel(const __grid_constant__ TokenParams q) {
+    const SsuParams &p = q.p;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const unsigned tile = blockIdx.x;
+    const int slab = static_cast<int>(tile % static_cast<unsigned>(p.slabs));
+    const unsigned unit = tile / static_cast<unsigned>(p.slabs);
+    const int h = static_cast<int>(unit % static_cast<unsigned>(p.nheads));
+    const long long b = static_cast<long long>(unit / static_cast<unsigned>(p.nheads));
+
+    const long long s = load_slot<kIdx64>(p, b);
+    if (s < 0 || s >= p.pool_size) {
+        if (h == 0 && slab == 0 && threadIdx.x == 0) record_skip(p, b);
+        return;
+    }
+    const int row0 = slab * p.rows_per_cta + warp * RPW;
+    float *srow = p.state + s * p.st_pool + h * p.st_head + row0 * p.st_row + lane * 4;
+
+    float4 v[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+        v[r] = row0 + r < p.headdim ? __ldcs(reinterpret_cast<const float4 *>(srow + r * p.st_row))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    const float bias = p.dt_bias[h * p.bias_h];
+    const float Ah = p.A[h * p.A_h];
+    const float Dh = p.D[h * p.D_h];
+    const int g = h / p.heads_per_group;
+    TokenIn cur = load_token<RPW>(q, b, h, g, row0, 0, lane);
+    for (int t = 0; t < q.tokens; ++t) {
+        TokenIn nxt = cur;
+        if (t + 1 < q.tokens) nxt = load_token<RPW>(q, b, h, g, row0, t + 1, lane);
+        const float dtv = softplus_f32(cur.dt + bias);
+        const float dA = expf(dtv * Ah);
+        float part[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float xr = __shfl_sync(0xffffffffu, cur.x, r);
+            part[r] = update_cols(v[r], dA, dtv * xr, cur.bb, cur.cc);
+        }
+        if (q.inter) {
+            float *irow = q.inter + b * q.in_b + t * q.in_t + h * q.in_h + row0 * q.in_p + lane * 4;
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+                if (row0 + r < p.headdim)
+                    __stcs(reinterpret_cast<float4 *>(irow + r * q.in_p), v[r]);
+        }
+        const float total = reduce_rows<RPW>(part, lane);
+        const int rl = row_of_lane<RPW>(lane);
+        const float xr = __shfl_sync(0xffffffffu, cur.x, rl);
+        if (writes_row<RPW>(lane) && row0 + rl < p.headdim)
+            p.out[b * p.out_b + t * q.out_t + h * p.out_h + row0 + rl] =
+                __float2bfloat16_rn(fmaf(Dh, xr, total));
+        cur = nxt;
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+        if (row0 + r < p.headdim) __stcs(reinterpret_cast<float4 *>(srow + r * p.st_row), v[r]);
+}
+
+template <bool kIdx64>
+cudaError_t launch_tokens(const TokenParams &q, int rpw, int wpc, unsigned grid,
+                          cudaStream_t st) {
+    const dim3 block(32 * wpc);
+    switch (rpw) {
+        case 1: ssu_tokens_kernel<1, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 2: ssu_tokens_kernel<2, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 4: ssu_tokens_kernel<4, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 8: ssu_tokens_kernel<8, kIdx64><<<grid, block, 0, st>>>(q); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, float *state_pool,
+                                          const void *state_batch_indices, const uint16_t *x,
+                                          const uint16_t *dt, const float *dt_bias,
+                                          const float *A, const uint16_t *B, const uint16_t *C,
+                                          const float *D, uint16_t *out, float *intermediate,
+                                          const ssu_shape_t *shape, const ssu_strides_t *strides,
+                                          int64_t tokens, const ssu_token_strides_t *ts,
+                                          ssu_stream_t stream) {
+    if (!handle) return fail(SSU_ERR_INVALID_ARG, "NULL handle");
+    if (!ts) return fail(SSU_ERR_INVALID_ARG, "token strides must not be NULL");
+    if (tokens < 1 || tokens > SSU_MAX_TOKENS)
+        return fail(SSU_ERR_INVALID_ARG, "tokens %lld outside 1..%d", (long long)tokens,
+                    SSU_MAX_TOKENS);
+    ssu_status_t st = validate_impl(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C,
+                                    D, out, shape, strides);
+    if (st != SSU_OK || shape->batch == 0) return st;
+    if (ts->x < 0 || ts->out < 0 || ts->dt < 0 || ts->B < 0 || ts->C < 0)
+        return fail(SSU_ERR_INVALID_ARG, "negative token stride");
+    if (intermediate) {
+        for (int j = 0; j < 5; ++j)
+            if (ts->intermediate[j] < 0) return fail(SSU_ERR_INVALID_ARG, "negative stride");
+        if (ts->intermediate[4] != 1)
+            return fail(SSU_ERR_UNSUPPORTED, "intermediate dstate-stride must be 1");
+        for (int j = 0; j < 4; ++j)
+            if (ts->intermediate[j] % 4)
+                return fail(SSU_ERR_MISALIGNED, "intermediate strides must be multiples of 4");
+        if (!aligned(intermediate, 16))
+            return fail(SSU_ERR_MISALIGNED, "intermediate is not 16-byte aligned");
+    }
+    const ssu_shape_t &s = *shape;
+    // 8 rows per warp and 2 warps per CTA, as the single-token table (fewer rows for a small
+    // headdim).
+    int rpw = 8;
+    while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
+    const int wpc = s.headdim >= 2 * rpw ? 2 : 1;
+    const int rows_per_tile = rpw * wpc;
+    const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
+    const long long tiles = s.batch * s.nheads * slabs;
+    if (tiles > INT_MAX) return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
+
+    TokenParams q{};
+    SsuParams &p = q.p;
+    p.state = state_pool;
+    p.idx = state_batch_indices;
+    p.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    p.dt = reinterpret_cast<const __nv_bfloat16 *>(dt);
+    p.dt_bias = dt_bias;
+    p.A = A;
+    p.B = reinterpret_cast<const __nv_bfloat16 *>(B);
+    p.C = reinterpret_cast<const __nv_bfloat16 *>(C);
+    p.D = D;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.st_pool = strides->state[0];
+    p.st_head = strides->state[1];
+    p.st_row = strides->state[2];
+    p.x_b = strides->x[0];
+    p.x_h = strides->x[1];
+    p.out_b = strides->out[0];
+    p.out_h = strides->out[1];
+    p.dt_b = strides->dt[0];
+    p.dt_h = strides->dt[1];
+    p.B_b = strides->B[0];
+    p.B_g = strides->B[1];
+    p.C_b = strides->C[0];
+    p.C_g = strides->C[1];
+    p.bias_h = strides->dt_bias[0];
+    p.D_h = strides->D[0];
+    p.A_h = strides->A[0];
+    p.idx_s = strides->idx;
+    p.pool_size = s.pool_size;
+    p.nheads = static_cast<int>(s.nheads);
+    p.headdim = static_cast<int>(s.headdim);
+    p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
+    p.slabs = static_cast<int>(slabs);
+    p.rows_per_cta = rows_per_tile;
+    p.err = handle->err;
+    q.inter = intermediate;
+    q.x_t = ts->x;
+    q.out_t = ts->out;
+    q.dt_t = ts->dt;
+    q.B_t = ts->B;
+    q.C_t = ts->C;
+    q.in_b = ts->intermediate[0];
+    q.in_t = ts->intermediate[1];
+    q.in_h = ts->intermediate[2];
+    q.in_p = ts->intermediate[3];
+    q.tokens = static_cast<int>(tokens);
+
+    DeviceGuard guard(handle->device);
+    if (guard.err != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        s.index_dtype == SSU_INDEX_I64
+            ? launch_tokens<true>(q, rpw, wpc, static_cast<unsigned>(tiles), cs)
+            : launch_tokens<false>(q, rpw, wpc, static_cast<unsigned>(tiles), cs);
+    if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+    return ok();
+}

@@ -110,3 +110,24 @@ def test_reference_arm_other_ranks_do_nothing():
     r = _run_bench(["--impl", "reference", "--steps", "3", "--warmup", "1"],
                    {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_copy_bytes_reproduce_the_copy_table():
+    # 2 x (49.875 MiB per request) x reqs / latency reproduces every GB/s the page prints.
+    table = json.loads((GOLDEN / "p2_copy_table.json").read_text())
+    per_req = bench.copy_bytes_per_request()
+    assert abs(per_req / 2 ** 20 - table["mib_per_request"]) < 0.01
+    for r in table["rows"]:
+        gbs = 2 * r["reqs"] * per_req / (r["us"] * 1e-6) / 1e9
+        assert abs(gbs / r["gbs"] - 1) < 0.003, r
+        assert bench.PAGE_COPY_GBS[r["reqs"]] == r["gbs"]
+
+
+def test_token_bytes_reduce_to_single_step():
+    # one token, no intermediate states: the single-step count
+    assert bench.bytes_per_call_tokens(128, 1, False) == bench.bytes_per_call(128)
+    # each extra token adds only its inputs and outputs; intermediates add T states
+    extra = bench.bytes_per_call_tokens(128, 2, False) - bench.bytes_per_call(128)
+    assert extra == 128 * (16 * 64 * 2 * 2 + 2 * 128 * 2 + 16 * 2)
+    assert (bench.bytes_per_call_tokens(128, 3, True) - bench.bytes_per_call_tokens(128, 3, False)
+            == 3 * 128 * 16 * 64 * 128 * 4)

@@ -327,3 +327,27 @@ def test_cold_l2_set_count():
     assert wl.sets_for_cold_l2(128, 16, l2) == 6
     assert wl.sets_for_cold_l2(8, 16, l2) == 95
     assert wl.sets_for_cold_l2(512, 16, l2, min_sets=3) == 3
+
+
+# ---- the state-block copy ----------------------------------------------------------------
+
+def test_copy_blocks_hand_case():
+    # Two tensors of 4 blocks; requests copy 0 -> 2 and 3 -> 1; block ids written out by hand.
+    a = np.arange(4 * 3, dtype=np.float32).reshape(4, 3)          # block k = [3k, 3k+1, 3k+2]
+    b = np.array([[10, 11], [20, 21], [30, 31], [40, 41]], dtype=np.uint16)
+    (na, nb), skipped = oracle.copy_blocks([a, b], [0, 3], [2, 1])
+    assert skipped == 0
+    np.testing.assert_array_equal(na, [[0, 1, 2], [9, 10, 11], [0, 1, 2], [9, 10, 11]])
+    np.testing.assert_array_equal(nb, [[10, 11], [40, 41], [10, 11], [40, 41]])
+    np.testing.assert_array_equal(a, np.arange(12).reshape(4, 3))  # inputs untouched
+
+
+def test_copy_blocks_skips_requests_out_of_any_range():
+    a = np.zeros((4, 2), dtype=np.float32)
+    b = np.ones((3, 2), dtype=np.float32)
+    a[1] = 5
+    (na, nb), skipped = oracle.copy_blocks([a, b], [1, 3, -1], [0, 2, 0])
+    # request 1 names block 3, valid in a but not in b: skipped for both tensors
+    assert skipped == 2
+    np.testing.assert_array_equal(na[0], [5, 5])
+    np.testing.assert_array_equal(na[2], [0, 0])

@@ -1,0 +1,175 @@
+"""GPU parity of the multi-token step (T consecutive tokens per request) against the oracle,
+which applies its pinned single step T times in order."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_update_02_gb300 as ssu
+import workloads as wl
+from parity_util import bf16_tensor, bits_of, check_state, check_y, expected_terms, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def op():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    o = ssu.SelectiveStateUpdate(0)
+    yield o
+    o.close()
+
+
+def _tokens_problem(bs, T, H=16, P=64, N=128, G=1, pool_size=None, seed=0):
+    pr = wl.make_problem(bs, H, P, N, G, pool_size=pool_size, seed=seed)
+    rng = np.random.default_rng(seed + 7)
+    steps = [wl.request_inputs(rng, bs, H, P, N, G) for _ in range(T)]
+    x = np.stack([s[0] for s in steps], 1)       # [bs, T, H, P]
+    dt = np.stack([s[1] for s in steps], 1)      # [bs, T, H]
+    B = np.stack([s[2] for s in steps], 1)       # [bs, T, G, N]
+    C = np.stack([s[3] for s in steps], 1)
+    return pr, x, dt, B, C
+
+
+def _run(op, pr, x, dt, B, C, idx=None, with_inter=True, idx_dtype=torch.int32):
+    dev = to_device(pr, "cuda", idx_dtype)
+    if idx is not None:
+        dev["state_batch_indices"] = torch.from_numpy(idx).to("cuda").to(idx_dtype)
+    bs, T, H, P = x.shape
+    out = torch.zeros(bs, T, H, P, dtype=torch.bfloat16, device="cuda")
+    inter = (torch.full((bs, T, H, P, pr.pool.shape[3]), 123.0, device="cuda")
+             if with_inter else None)
+    op.tokens(dev["state_pool"], dev["state_batch_indices"], bf16_tensor(x, "cuda"),
+              bf16_tensor(dt, "cuda"), dev["dt_bias"], dev["A"], bf16_tensor(B, "cuda"),
+              bf16_tensor(C, "cuda"), dev["D"], out, inter)
+    torch.cuda.synchronize()
+    return dev["state_pool"].cpu().numpy(), bits_of(out), (inter.cpu().numpy()
+                                                           if with_inter else None)
+
+
+def _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter, idx=None):
+    idx = pr.idx if idx is None else idx
+    ref_pool, ref_y, ref_inter, skipped = oracle.ssu_tokens(pr.pool, idx, x, dt, pr.dt_bias,
+                                                           pr.A, B, C, pr.D, pr.ngroups)
+    ok = (idx >= 0) & (idx < pr.pool_size)
+    check_state(got_pool[idx[ok]], ref_pool[idx[ok]])
+    untouched = np.setdiff1d(np.arange(pr.pool_size), idx[ok])
+    assert np.array_equal(got_pool[untouched], pr.pool[untouched])
+    T = x.shape[1]
+    for t in range(T):
+        Ch, Dx = expected_terms(x[ok, t], pr.D, C[ok, t], pr.ngroups, pr.nheads)
+        check_y(got_out[ok, t], ref_y[ok, t], ref_inter[ok, t], Ch, Dx, pr.pool.shape[3],
+                f"y token {t}")
+        if got_inter is not None:
+            check_state(got_inter[ok, t], ref_inter[ok, t], f"intermediate token {t}")
+    return skipped
+
+
+def test_one_token_equals_ssu_update_bitwise(op):
+    pr, x, dt, B, C = _tokens_problem(12, 1, seed=1)
+    got_pool, got_out, _ = _run(op, pr, x, dt, B, C, with_inter=False)
+    ref = to_device(pr, "cuda")
+    ref["x"], ref["dt"] = bf16_tensor(x[:, 0], "cuda"), bf16_tensor(dt[:, 0], "cuda")
+    ref["B"], ref["C"] = bf16_tensor(B[:, 0], "cuda"), bf16_tensor(C[:, 0], "cuda")
+    op(ref["state_pool"], ref["state_batch_indices"], ref["x"], ref["dt"], ref["dt_bias"],
+       ref["A"], ref["B"], ref["C"], ref["D"], ref["out"])
+    torch.cuda.synchronize()
+    assert np.array_equal(got_pool, ref["state_pool"].cpu().numpy())
+    assert np.array_equal(got_out[:, 0], bits_of(ref["out"]))
+
+
+@pytest.mark.parametrize("T", [2, 3, 4, 8])
+@pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
+def test_tokens_match_oracle(op, T, idx_dtype):
+    pr, x, dt, B, C = _tokens_problem(10, T, seed=T)
+    got = _run(op, pr, x, dt, B, C, idx_dtype=idx_dtype)
+    assert _check_all(pr, x, dt, B, C, *got) == 0
+    assert op.get_error() == (0, -1)
+
+
+@pytest.mark.parametrize("P,G", [(40, 1), (3, 2), (100, 4)])
+def test_tokens_ragged_headdim_and_groups(op, P, G):
+    pr, x, dt, B, C = _tokens_problem(6, 3, H=8, P=P, G=G, seed=P)
+    got = _run(op, pr, x, dt, B, C)
+    _check_all(pr, x, dt, B, C, *got)
+
+
+def test_tokens_without_intermediate(op):
+    pr, x, dt, B, C = _tokens_problem(9, 3, seed=11)
+    got_pool, got_out, _ = _run(op, pr, x, dt, B, C, with_inter=False)
+    _check_all(pr, x, dt, B, C, got_pool, got_out, None)
+
+
+def test_tokens_skip_out_of_range_requests(op):
+    pr, x, dt, B, C = _tokens_problem(8, 3, pool_size=12, seed=5)
+    idx = pr.idx.copy()
+    idx[[2, 6]] = [12, -3]
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, idx=idx)
+    assert _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter, idx) == 2
+    assert op.get_error() == (2, 2)
+    assert (got_inter[[2, 6]] == 123.0).all() and (got_out[[2, 6]] == 0).all()
+
+
+def test_tokens_strided_views(op):
+    # x, B, C of every token as views into one packed [bs, T, H*P + 2N] bf16 tensor; dt as a
+    # head-expanded stride-0 view; per-head operands expanded as in ssu_update's tests.
+    bs, T, H, P, N = 7, 3, 16, 64, 128
+    pr, _, _, _, _ = _tokens_problem(bs, 1, seed=21)
+    rng = np.random.default_rng(22)
+    packed = wl.f32_to_bf16_bits(rng.standard_normal((bs, T, H * P + 2 * N), dtype=np.float32))
+    dt = wl.f32_to_bf16_bits(rng.uniform(-4, 0, (bs, T, H)).astype(np.float32))
+    pk = bf16_tensor(packed, "cuda")
+    xv = pk[:, :, :H * P].view(bs, T, H, P)
+    Bv = pk[:, :, H * P:H * P + N].unsqueeze(2)
+    Cv = pk[:, :, H * P + N:].unsqueeze(2)
+    dtv = bf16_tensor(dt, "cuda").unsqueeze(-1).expand(bs, T, H, P)
+    dev = to_device(pr, "cuda")
+    out = torch.zeros(bs, T, H, P, dtype=torch.bfloat16, device="cuda")
+    op.tokens(dev["state_pool"], dev["state_batch_indices"], xv, dtv,
+              dev["dt_bias"].unsqueeze(-1).expand(H, P), dev["A"][:, None, None].expand(H, P, N),
+              Bv, Cv, dev["D"].unsqueeze(-1).expand(H, P), out)
+    torch.cuda.synchronize()
+    x = packed[:, :, :H * P].reshape(bs, T, H, P)
+    B = packed[:, :, H * P:H * P + N].reshape(bs, T, 1, N)
+    C = packed[:, :, H * P + N:].reshape(bs, T, 1, N)
+    _check_all(pr, x, dt, B, C, dev["state_pool"].cpu().numpy(), bits_of(out), None)
+
+
+def test_tokens_serving_batch_128_sampled(op):
+    # batch 128, 16 heads, 3 tokens per request (one verified token plus two drafts), a
+    # 2432-slot pool; sampled requests against the oracle, untouched slots bit-identical.
+    bs, T, H = 128, 3, 16
+    rng = np.random.default_rng(3)
+    pool = wl.state_pool(rng, 2432, H)
+    idx = wl.rotation_sets(bs, 19, seed=3)[4]
+    dt_bias, A, D = wl.head_params(rng, H)
+    steps = [wl.request_inputs(rng, bs, H) for _ in range(T)]
+    x, dt, B, C = (np.stack([s[k] for s in steps], 1) for k in range(4))
+    pool_d = torch.from_numpy(pool).cuda()
+    out = torch.zeros(bs, T, H, 64, dtype=torch.bfloat16, device="cuda")
+    inter = torch.empty(bs, T, H, 64, 128, device="cuda")
+    op.tokens(pool_d, torch.from_numpy(idx).cuda(), bf16_tensor(x, "cuda"), bf16_tensor(dt, "cuda"),
+              torch.from_numpy(dt_bias).cuda(), torch.from_numpy(A).cuda(), bf16_tensor(B, "cuda"),
+              bf16_tensor(C, "cuda"), torch.from_numpy(D).cuda(), out, inter)
+    torch.cuda.synchronize()
+    rows = np.array([0, 17, 64, 127])
+    sub = pool[idx[rows]]
+    ref_pool, ref_y, ref_inter, _ = oracle.ssu_tokens(sub, np.arange(len(rows)), x[rows],
+                                                     dt[rows], dt_bias, A, B[rows], C[rows], D)
+    got_pool = pool_d[torch.from_numpy(idx[rows]).cuda()].cpu().numpy()
+    check_state(got_pool, ref_pool)
+    got_inter = inter[torch.from_numpy(rows).cuda()].cpu().numpy()
+    got_out = bits_of(out)[rows]
+    for t in range(T):
+        check_state(got_inter[:, t], ref_inter[:, t])
+        Ch, Dx = expected_terms(x[rows, t], D, C[rows, t], 1, H)
+        check_y(got_out[:, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, 128)
+    mask = np.ones(2432, bool)
+    mask[idx] = False
+    keep = torch.from_numpy(np.nonzero(mask)[0]).cuda()
+    assert torch.equal(pool_d[keep], torch.from_numpy(pool[mask]).cuda())
+
