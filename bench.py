@@ -46,16 +46,17 @@ NOMINAL_HBM_GBS = 8000.0     # the pages' round GB200/B200 HBM3e figure
 FALLBACK_HBM_GBS = 6800.0
 PAGE_US = {8: 4.02, 128: 24.1, 512: 85.7}   # sglang PR #41223 Speedup Result, B200 (context)
 CSRC = ROOT / "selective_state_update_02_gb300" / "csrc"
-KERNEL_SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_device.cuh"]
+KERNEL_SOURCES = [CSRC / "ssu_vec.cuh", CSRC / "ssu_device.cuh"]     # VEC kernel
+BULK_SOURCES = [CSRC / "ssu_bulk.cuh", CSRC / "ssu_device.cuh"]      # BULK kernel
 
 
 # ---- arithmetic of the measurement (host logic, tested on CPU) ---------------------------
 
 def bytes_per_call(bs: int, H: int = NHEADS, P: int = HEADDIM, N: int = DSTATE,
-                   G: int = NGROUPS, idx_bytes: int = 4) -> int:
+                   G: int = NGROUPS, idx_bytes: int = 4, state_bytes: int = 4) -> int:
     """Algorithmic HBM bytes of one call: the state read and written once, every input read
     once, the output written once; per-head parameters counted once (stride-0 broadcasts)."""
-    state = 2 * bs * H * P * N * 4
+    state = 2 * bs * H * P * N * state_bytes
     x = bs * H * P * 2
     y = bs * H * P * 2
     bc = 2 * bs * G * N * 2
@@ -70,11 +71,12 @@ def flops_per_call(bs: int, H: int = NHEADS, P: int = HEADDIM, N: int = DSTATE) 
     return 5 * bs * H * P * N
 
 
-def sets_for(bs: int, H: int, l2_bytes: int) -> int:
+def sets_for(bs: int, H: int, l2_bytes: int, N: int = DSTATE, elem_bytes: int = 4) -> int:
     import workloads as wl
-    if bs == DEFAULT_BATCH and H == NHEADS:
-        return max(SERVING_SETS, wl.sets_for_cold_l2(bs, H, l2_bytes))
-    return wl.sets_for_cold_l2(bs, H, l2_bytes)
+    n = wl.sets_for_cold_l2(bs, H, l2_bytes, N=N, elem_bytes=elem_bytes)
+    if bs == DEFAULT_BATCH and H == NHEADS and N == DSTATE and elem_bytes == 4:
+        return max(SERVING_SETS, n)
+    return n
 
 
 def load_peaks() -> dict:
@@ -86,21 +88,21 @@ def load_peaks() -> dict:
 
 
 def source_digest(files=None) -> str:
-    """Digest of the sources that define the timed kernel (its translation unit and the
-    device header it includes): counters taken on other sources are not reported."""
+    """Digest of the sources that define the timed kernel (its own header and the device
+    helpers it includes): counters taken on other sources are not reported."""
     h = hashlib.sha256()
     for f in files or KERNEL_SOURCES:
         h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_tag: str) -> int | None:
+def recorded_traffic(workload_tag: str, bulk: bool = False) -> int | None:
     """DRAM bytes per launch from a committed ncu summary, if it was taken on this source.
 
     The summaries under profiles/ carry a line
     ``traffic_per_launch_bytes: <int> source: <digest> workload: <tag>``.
     """
-    digest = source_digest()
+    digest = source_digest(BULK_SOURCES if bulk else KERNEL_SOURCES)
     for f in sorted((ROOT / "profiles").glob("*.md")):
         for m in re.finditer(r"traffic_per_launch_bytes:\s*(\d+)\s+source:\s*([0-9a-f]+)\s+"
                              r"workload:\s*(\S+)", f.read_text()):
@@ -190,27 +192,32 @@ class ClockSampler:
 class Workload:
     """Device-resident rotation workload for one batch size."""
 
-    def __init__(self, bs: int, H: int, dev, seed: int, l2_bytes: int, packed: bool = False):
+    def __init__(self, bs: int, H: int, dev, seed: int, l2_bytes: int, packed: bool = False,
+                 N: int = DSTATE, state_dtype: str = "f32"):
         import torch
 
         import selective_state_update_02_gb300 as ssu
         import workloads as wl
-        self.bs, self.H = bs, H
-        self.n_sets = sets_for(bs, H, l2_bytes)
+        self.bs, self.H, self.N = bs, H, N
+        self.elem_bytes = 2 if state_dtype == "bf16" else 4
+        self.n_sets = sets_for(bs, H, l2_bytes, N, self.elem_bytes)
         rng = np.random.default_rng(seed)
-        pool = wl.state_pool(rng, bs * self.n_sets, H)
-        self.pool = torch.from_numpy(pool).to(dev)
+        pool = wl.state_pool(rng, bs * self.n_sets, H, N=N, dtype=state_dtype)
+        if state_dtype == "bf16":
+            self.pool = torch.from_numpy(pool.view(np.int16)).view(torch.bfloat16).to(dev)
+        else:
+            self.pool = torch.from_numpy(pool).to(dev)
         del pool
         self.sets = torch.from_numpy(wl.rotation_sets(bs, self.n_sets, seed).astype(np.int32)) \
             .to(dev)
         dt_bias, A, D = wl.head_params(rng, H)
         self.dt_bias = torch.from_numpy(dt_bias).to(dev).unsqueeze(-1).expand(H, HEADDIM)
-        self.A = torch.from_numpy(A).to(dev)[:, None, None].expand(H, HEADDIM, DSTATE)
+        self.A = torch.from_numpy(A).to(dev)[:, None, None].expand(H, HEADDIM, N)
         self.D = torch.from_numpy(D).to(dev).unsqueeze(-1).expand(H, HEADDIM)
         # per set: x, B, C as strided views of one packed bf16 tensor, dt head-expanded
-        width = H * HEADDIM + 2 * NGROUPS * DSTATE
+        width = H * HEADDIM + 2 * NGROUPS * N
         self.packed = torch.from_numpy(
-            wl.packed_xbc(rng, bs * self.n_sets, H).view(np.int16)).view(torch.bfloat16) \
+            wl.packed_xbc(rng, bs * self.n_sets, H, N=N).view(np.int16)).view(torch.bfloat16) \
             .to(dev).view(self.n_sets, bs, width)
         self.dt = torch.from_numpy(wl.f32_to_bf16_bits(
             rng.uniform(-4, 0, (self.n_sets, bs, H)).astype(np.float32)).view(np.int16)) \
@@ -220,8 +227,8 @@ class Workload:
         for k in range(self.n_sets):
             pk = self.packed[k]
             x = pk[:, :H * HEADDIM].view(bs, H, HEADDIM)
-            B = pk[:, H * HEADDIM:H * HEADDIM + DSTATE].unsqueeze(1)
-            C = pk[:, H * HEADDIM + DSTATE:].unsqueeze(1)
+            B = pk[:, H * HEADDIM:H * HEADDIM + N].unsqueeze(1)
+            C = pk[:, H * HEADDIM + N:].unsqueeze(1)
             dt = self.dt[k].unsqueeze(-1).expand(bs, H, HEADDIM)
             tensors = (self.pool, self.sets[k], x, dt, self.dt_bias, self.A, B, C, self.D,
                        self.out[k])
@@ -295,8 +302,8 @@ def time_e2e(wl_, handle, steps: int, dev) -> dict:
     import torch
 
     import selective_state_update_02_gb300 as ssu
-    bs, H = wl_.bs, wl_.H
-    width = H * HEADDIM + 2 * DSTATE
+    bs, H, N = wl_.bs, wl_.H, wl_.N
+    width = H * HEADDIM + 2 * N
     # one pinned staging buffer per step input set: [idx int32 | packed x/B/C | dt] as bytes
     n_idx, n_xbc, n_dt = bs * 4, bs * width * 2, bs * H * 2
     step_bytes = n_idx + n_xbc + n_dt
@@ -311,8 +318,8 @@ def time_e2e(wl_, handle, steps: int, dev) -> dict:
     dt = dev_in[n_idx + n_xbc:].view(torch.bfloat16).view(bs, H).unsqueeze(-1) \
         .expand(bs, H, HEADDIM)
     x = pk[:, :H * HEADDIM].view(bs, H, HEADDIM)
-    B = pk[:, H * HEADDIM:H * HEADDIM + DSTATE].unsqueeze(1)
-    C = pk[:, H * HEADDIM + DSTATE:].unsqueeze(1)
+    B = pk[:, H * HEADDIM:H * HEADDIM + N].unsqueeze(1)
+    C = pk[:, H * HEADDIM + N:].unsqueeze(1)
     out = torch.empty(bs, H, HEADDIM, dtype=torch.bfloat16, device=dev)
     host_out = torch.empty(wl_.n_sets, bs, H, HEADDIM, dtype=torch.bfloat16, pin_memory=True)
     stream = torch.cuda.Stream()
@@ -426,15 +433,16 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def config_for(bs: int, n_sets: int) -> dict:
+def config_for(bs: int, n_sets: int, N: int = DSTATE, state_dtype: str = "f32") -> dict:
+    eb = 2 if state_dtype == "bf16" else 4
     return {"workload": f"decode step, batch {bs}, {NHEADS} heads, headdim {HEADDIM}, dstate "
-                        f"{DSTATE}, fp32 state pool of {bs * n_sets} slots in {n_sets} disjoint "
-                        f"{bs}-slot rotation sets; x/B/C strided views of one packed bf16 "
-                        f"tensor, dt/A/D/dt_bias stride-0 broadcasts",
-            "batch": bs, "nheads": NHEADS, "headdim": HEADDIM, "dstate": DSTATE,
-            "ngroups": NGROUPS, "pool_slots": bs * n_sets,
+                        f"{N}, {state_dtype} state pool of {bs * n_sets} slots in {n_sets} "
+                        f"disjoint {bs}-slot rotation sets; x/B/C strided views of one packed "
+                        f"bf16 tensor, dt/A/D/dt_bias stride-0 broadcasts",
+            "batch": bs, "nheads": NHEADS, "headdim": HEADDIM, "dstate": N,
+            "state_dtype": state_dtype, "ngroups": NGROUPS, "pool_slots": bs * n_sets,
             "l2": f"inputs larger than L2: call i touches set i mod {n_sets}; the sets hold "
-                  f"{bs * n_sets * NHEADS * HEADDIM * DSTATE * 4 / 2 ** 20:.0f} MiB of state"}
+                  f"{bs * n_sets * NHEADS * HEADDIM * N * eb / 2 ** 20:.0f} MiB of state"}
 
 
 def run_ours(args) -> None:
@@ -456,7 +464,10 @@ def run_ours(args) -> None:
         ssu.ssu_set_launch(handle, *[int(v) for v in args.launch.split(",")])
     warmup = max(args.warmup, 3)
     bs = args.batch
-    main = Workload(bs, NHEADS, dev, seed=rank, l2_bytes=l2, packed=True)
+    N, sdt = args.dstate, args.state_dtype
+    eb = 2 if sdt == "bf16" else 4
+    default_workload = N == DSTATE and sdt == "f32"
+    main = Workload(bs, NHEADS, dev, seed=rank, l2_bytes=l2, packed=True, N=N, state_dtype=sdt)
 
     def barrier():
         if world > 1:
@@ -470,20 +481,23 @@ def run_ours(args) -> None:
     value = aggregate_value(per_rank, args.steps)
     per_launch_us = max(per_rank) / args.steps
     peaks = load_peaks()
-    bpc = bytes_per_call(bs)
+    bpc = bytes_per_call(bs, N=N, state_bytes=eb)
     achieved_gbs = bpc / (per_launch_us * 1e-6) / 1e9
     launch = ssu.ssu_get_launch(handle, main.args[0][1])
     tag = f"batch{bs}" + ("-bulk" if launch[0] == 2 else "")
-    traffic = recorded_traffic(tag)
+    if not default_workload:
+        tag += f"-n{N}-{sdt}"
+    traffic = recorded_traffic(tag, bulk=launch[0] == 2)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": untimed, "ms_per_step": round(value / 1000.0, 6),
         "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": round(value / PAGE_US[bs], 4) if bs in PAGE_US and world == 1 else None,
+        "vs_baseline": (round(value / PAGE_US[bs], 4)
+                        if bs in PAGE_US and world == 1 and default_workload else None),
         "vs_baseline_note": "value / the pages' B200 Triton time for this batch (another "
                             "machine: context, not the target)",
         "dtype": "f32", "data": "synthetic",
-        "config": config_for(bs, main.n_sets) | {
+        "config": config_for(bs, main.n_sets, N, sdt) | {
             "launch": {"mode": launch[0], "rows_per_warp": launch[1],
                        "warps_per_cta": launch[2], "stages": launch[3]}},
         "achieved_tbps": round(achieved_gbs / 1000.0, 3),
@@ -498,13 +512,13 @@ def run_ours(args) -> None:
         "clocks": clocks,
     }
     if not args.skip_ceiling:
-        state_bytes = bs * NHEADS * HEADDIM * DSTATE * 4
+        state_bytes = bs * NHEADS * HEADDIM * N * eb
         t_in = same_size_ceiling(state_bytes, dev, l2)
         ceil_gbs = 2 * state_bytes / (t_in * 1e-6) / 1e9
         line["roofline"]["same_size_inplace_gbs"] = round(ceil_gbs, 1)
         line["roofline"]["frac_of_same_size_inplace"] = round(
             (2 * state_bytes / (per_launch_us * 1e-6) / 1e9) / ceil_gbs, 4)
-    if not args.skip_extra and world == 1:
+    if not args.skip_extra and world == 1 and default_workload:
         by = {}
         for b in (8, 128, 512):
             if b == bs:
@@ -789,15 +803,21 @@ def run_sweep(args) -> None:
     handle = ssu.ssu_create(0)
     best = {}
     for bs in args.sweep_batches:
-        w = Workload(bs, NHEADS, dev, seed=200 + bs, l2_bytes=l2)
+        N, sdt = args.dstate, args.state_dtype
+        eb = 2 if sdt == "bf16" else 4
+        w = Workload(bs, NHEADS, dev, seed=200 + bs, l2_bytes=l2, N=N, state_dtype=sdt)
+        shapes = SWEEP_SHAPES
+        if N != DSTATE or sdt != "f32":   # BULK and 16 rows per warp: fp32, dstate 128 only
+            shapes = [sh for sh in SWEEP_SHAPES if sh[0] == 1 and sh[1] <= 8]
         n = max(1000, int(args.sweep_us_budget / (0.16 * bs + 2.0)))
-        for mode, rpw, wpc, stages in SWEEP_SHAPES:
+        for mode, rpw, wpc, stages in shapes:
             ssu.ssu_set_launch(handle, mode, rpw, wpc, stages)
             ms, _, _ = time_calls(w, handle, n, 5)
             us = ms * 1000.0 / n
             rec = {"batch": bs, "mode": "vec" if mode == 1 else "bulk", "rows_per_warp": rpw,
                    "warps_per_cta": wpc, "stages": stages, "us_per_call": round(us, 3),
-                   "tbps": round(bytes_per_call(bs) / (us * 1e-6) / 1e12, 3), "steps": n}
+                   "tbps": round(bytes_per_call(bs, N=N, state_bytes=eb) / (us * 1e-6) / 1e12, 3),
+                   "steps": n, "dstate": N, "state_dtype": sdt}
             print(json.dumps(rec), flush=True)
             if bs not in best or us < best[bs]["us_per_call"]:
                 best[bs] = rec
@@ -820,6 +840,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=DEFAULT_BATCH, choices=[8, 128, 512])
+    ap.add_argument("--dstate", type=int, default=DSTATE, choices=[64, 128, 256])
+    ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--e2e-steps", type=int, default=5000)
     ap.add_argument("--skip-extra", action="store_true", help="skip the batch 8/512 lines")
     ap.add_argument("--skip-e2e", action="store_true")

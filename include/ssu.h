@@ -13,8 +13,9 @@
  *     S[p,n]   = S[p,n] * dA + (dtv * x[b,h,p]) * B[b,g,n]  in place in state_pool[s,h]
  *     out[b,h,p] = bf16_rne( sum_n S[p,n] * C[b,g,n] + D[h] * x[b,h,p] )
  *
- * Types.  The state pool is fp32.  x, dt, B, C and out are bfloat16, passed as uint16_t
- * pointers to their bit patterns.  dt_bias, A and D are fp32.  state_batch_indices is int32
+ * Types.  The state pool is fp32 or bf16 (ssu_shape_t.state_dtype; either way the update runs in
+ * fp32 and a bf16 state is rounded to nearest even when stored).  x, dt, B, C and out are
+ * bfloat16, passed as uint16_t pointers to their bit patterns.  dt_bias, A and D are fp32.  state_batch_indices is int32
  * or int64 (ssu_shape_t.index_dtype).  All data pointers are DEVICE pointers on the handle's
  * device; the caller owns every buffer.  Sizes and strides are in ELEMENTS (not bytes).
  *
@@ -62,16 +63,19 @@ typedef enum {
 
 typedef enum { SSU_INDEX_I32 = 0, SSU_INDEX_I64 = 1 } ssu_index_dtype_t;
 
+/* Element type of the state pool (and of the multi-token intermediate states). */
+typedef enum { SSU_STATE_F32 = 0, SSU_STATE_BF16 = 1 } ssu_state_dtype_t;
+
 /* Problem sizes of one call. */
 typedef struct {
     int64_t batch;       /* bs: requests in this step; 0 is valid and enqueues nothing */
     int64_t nheads;      /* H >= 1 */
     int64_t headdim;     /* P >= 1 */
-    int64_t dstate;      /* N: this build implements N = 128 */
+    int64_t dstate;      /* N: 64, 128 or 256 */
     int64_t ngroups;     /* G >= 1 with H % G == 0; head h reads group h / (H / G) */
     int64_t pool_size;   /* slots in state_pool; valid slot ids are [0, pool_size) */
     int32_t index_dtype; /* ssu_index_dtype_t of state_batch_indices */
-    int32_t reserved;    /* set to 0 */
+    int32_t state_dtype; /* ssu_state_dtype_t of state_pool (0 = fp32) */
 } ssu_shape_t;
 
 /*
@@ -81,7 +85,7 @@ typedef struct {
  */
 typedef struct {
     int64_t state[4];   /* state_pool [pool, H, P, N]: N-stride must be 1; the other three
-                           must be multiples of 4 (16-byte rows) */
+                           must be multiples of 16 bytes (4 fp32 or 8 bf16 elements) */
     int64_t x[3];       /* x   [bs, H, P]: P-stride must be 1 */
     int64_t out[3];     /* out [bs, H, P]: P-stride must be 1 */
     int64_t dt[3];      /* dt  [bs, H, P]: P-stride must be 0 (one value per head) */
@@ -98,15 +102,16 @@ typedef enum {
     SSU_MODE_AUTO = 0,   /* use the built-in table (the default) */
     SSU_MODE_VEC = 1,    /* one CTA per tile; 16-byte vector loads/stores through registers */
     SSU_MODE_BULK = 2    /* persistent CTAs; bulk asynchronous copies (TMA engine) of whole
-                            tiles through a ring of shared-memory stages.  Needs contiguous
-                            state rows (state row stride == dstate); the table falls back to
-                            VEC otherwise, a forced BULK shape returns SSU_ERR_UNSUPPORTED */
+                            tiles through a ring of shared-memory stages.  fp32 state, dstate
+                            128, contiguous rows (row stride == dstate) only; a forced BULK
+                            shape returns SSU_ERR_UNSUPPORTED otherwise */
 } ssu_mode_t;
 
 /* A tile is rows_per_warp * warps_per_cta consecutive state rows of one (request, head). */
 typedef struct {
     int32_t mode;          /* ssu_mode_t */
-    int32_t rows_per_warp; /* rows each warp updates per tile: VEC 1,2,4,8,16; BULK 2,4,8,16 */
+    int32_t rows_per_warp; /* rows each warp updates per tile: VEC 1,2,4,8 (16 for an fp32
+                              state of dstate 128); BULK 2,4,8,16 */
     int32_t warps_per_cta; /* VEC: 1..16 warps; BULK: 1..8 compute warps (plus one producer) */
     int32_t stages;        /* BULK: shared-memory ring depth, 2..8 (stages x tile <= the
                               device's shared memory per CTA); VEC: ignored */
@@ -136,7 +141,7 @@ ssu_status_t ssu_destroy(ssu_handle_t handle);
  * Host-side validation of one call, exactly as ssu_update performs it, without a handle or a
  * device: pointers are checked for NULL and alignment only, never dereferenced.
  */
-ssu_status_t ssu_validate(const float *state_pool, const void *state_batch_indices,
+ssu_status_t ssu_validate(const void *state_pool, const void *state_batch_indices,
                           const uint16_t *x, const uint16_t *dt, const float *dt_bias,
                           const float *A, const uint16_t *B, const uint16_t *C, const float *D,
                           const uint16_t *out, const ssu_shape_t *shape,
@@ -148,7 +153,7 @@ ssu_status_t ssu_validate(const float *state_pool, const void *state_batch_indic
  * out.  Enqueued on `stream`; returns once enqueued.  Slots that no request names are never
  * read or written.  See the file header for the arithmetic and the error behaviour.
  */
-ssu_status_t ssu_update(ssu_handle_t handle, float *state_pool, const void *state_batch_indices,
+ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state_batch_indices,
                         const uint16_t *x, const uint16_t *dt, const float *dt_bias,
                         const float *A, const uint16_t *B, const uint16_t *C, const float *D,
                         uint16_t *out, const ssu_shape_t *shape, const ssu_strides_t *strides,
@@ -184,7 +189,7 @@ ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
  *     dtv = softplus(dt[b,t,h] + dt_bias[h]);   dA = exp(dtv * A[h])
  *     S[p,n] = S[p,n] * dA + (dtv * x[b,t,h,p]) * B[b,t,g,n]
  *     out[b,t,h,p] = bf16_rne( sum_n S[p,n] * C[b,t,g,n] + D[h] * x[b,t,h,p] )
- *     if intermediate: intermediate[b,t,h,p,n] = S[p,n]        (fp32)
+ *     if intermediate: intermediate[b,t,h,p,n] = S[p,n]        (the state's dtype)
  *   state_pool[s,h] = S
  *
  * The state is read once and written once per call, whatever T; with T = 1 and no
@@ -195,7 +200,8 @@ ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
 typedef struct {
     int64_t x, out, dt, B, C;  /* stride of the token index t in x, out, dt, B and C; the
                                   other strides come from ssu_strides_t */
-    int64_t intermediate[5];   /* [bs, T, H, P, N]: N-stride 1, the others multiples of 4 */
+    int64_t intermediate[5];   /* [bs, T, H, P, N]: N-stride 1, the others multiples of 16
+                                  bytes */
 } ssu_token_strides_t;
 
 #define SSU_MAX_TOKENS 64
@@ -203,14 +209,15 @@ typedef struct {
 /*
  * T consecutive decode steps (1 <= T <= SSU_MAX_TOKENS).  Pointers, shape and ssu_strides_t as
  * for ssu_update (describing token 0), plus `tokens` = T, the token strides, and
- * `intermediate` (device fp32, 16-byte aligned, or NULL for none).  Same error behaviour as
+ * `intermediate` (device buffer of the state's dtype, 16-byte aligned, or NULL for none).
+ * Within a call the running state stays in fp32; a bf16 state is rounded only when written.  Same error behaviour as
  * ssu_update; enqueued on `stream`; allocates and synchronises nothing.
  */
-ssu_status_t ssu_update_tokens(ssu_handle_t handle, float *state_pool,
+ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                                const void *state_batch_indices, const uint16_t *x,
                                const uint16_t *dt, const float *dt_bias, const float *A,
                                const uint16_t *B, const uint16_t *C, const float *D,
-                               uint16_t *out, float *intermediate, const ssu_shape_t *shape,
+                               uint16_t *out, void *intermediate, const ssu_shape_t *shape,
                                const ssu_strides_t *strides, int64_t tokens,
                                const ssu_token_strides_t *token_strides, ssu_stream_t stream);
 
@@ -288,7 +295,7 @@ ssu_status_t ssu_copy_set_launch(ssu_handle_t handle, const ssu_copy_launch_t *l
  */
 #define SSU_STATIC_SCRATCH_BYTES 256
 #define SSU_STATIC_MAX_BATCH 2147483647LL
-ssu_status_t ssu_update_static(float *state_pool, const void *state_batch_indices,
+ssu_status_t ssu_update_static(void *state_pool, const void *state_batch_indices,
                                const uint16_t *x, const uint16_t *dt, const float *dt_bias,
                                const float *A, const uint16_t *B, const uint16_t *C,
                                const float *D, uint16_t *out, const ssu_shape_t *shape,

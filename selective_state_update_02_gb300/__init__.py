@@ -5,8 +5,8 @@ the C names and only marshal arguments: tensor pointers, sizes and element strid
 the ABI structs, and every step of the update runs in the library's CUDA kernels.  There is
 no CPU or PyTorch fallback: if the library is missing, every entry point raises.
 
-Operand layout (sglang PR #41223, Details / Kernel measurement): ``state_pool`` fp32
-``[pool, H, P, N]``; ``state_batch_indices`` int32/int64 ``[bs]``; ``x`` and ``out`` bf16
+Operand layout (sglang PR #41223, Details / Kernel measurement): ``state_pool`` fp32 or bf16
+``[pool, H, P, N]`` (N = 64, 128 or 256); ``state_batch_indices`` int32/int64 ``[bs]``; ``x`` and ``out`` bf16
 ``[bs, H, P]``; ``B`` and ``C`` bf16 ``[bs, G, N]``; ``dt`` bf16 ``[bs, H]`` (or the
 head-expanded ``[bs, H, P]`` view with stride 0 over P); ``dt_bias`` and ``D`` fp32 ``[H]``
 (or ``[H, P]`` with stride 0); ``A`` fp32 ``[H]`` (or ``[H, P, N]`` with strides 0).
@@ -34,6 +34,9 @@ SSU_ERR_TIMEOUT = 6
 SSU_INDEX_I32 = 0
 SSU_INDEX_I64 = 1
 
+SSU_STATE_F32 = 0
+SSU_STATE_BF16 = 1
+
 SSU_MODE_AUTO = 0
 SSU_MODE_VEC = 1
 SSU_MODE_BULK = 2
@@ -44,7 +47,7 @@ _i64 = ctypes.c_int64
 class ssu_shape_t(ctypes.Structure):
     _fields_ = [("batch", _i64), ("nheads", _i64), ("headdim", _i64), ("dstate", _i64),
                 ("ngroups", _i64), ("pool_size", _i64), ("index_dtype", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("state_dtype", ctypes.c_int32)]
 
 
 class ssu_strides_t(ctypes.Structure):
@@ -183,7 +186,9 @@ def _broadcast_strides(t: torch.Tensor, name: str, dims: tuple[int, ...], full: 
 
 def describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out):
     """Build ``(ssu_shape_t, ssu_strides_t)`` for a set of tensors (no data is touched)."""
-    _expect(state_pool, "state_pool", torch.float32, (4,))
+    if not isinstance(state_pool, torch.Tensor) or state_pool.dim() != 4 or \
+            state_pool.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("state_pool must be a 4-D float32 or bfloat16 tensor")
     if state_batch_indices.dtype not in (torch.int32, torch.int64) or \
             state_batch_indices.dim() != 1:
         raise TypeError("state_batch_indices must be a 1-D int32 or int64 tensor")
@@ -208,7 +213,8 @@ def describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out):
         raise ValueError("dt must be [bs, H] or [bs, H, P]")
     shape = ssu_shape_t(bs, H, P, N, G, pool,
                         SSU_INDEX_I64 if state_batch_indices.dtype == torch.int64
-                        else SSU_INDEX_I32, 0)
+                        else SSU_INDEX_I32,
+                        SSU_STATE_BF16 if state_pool.dtype == torch.bfloat16 else SSU_STATE_F32)
     st = ssu_strides_t()
     st.state[:] = list(state_pool.stride())
     st.x[:] = list(x.stride())
@@ -323,8 +329,8 @@ def ssu_update_tokens(handle: int, state_pool, state_batch_indices, x, dt, dt_bi
                       out, intermediate=None, stream=None) -> None:
     """T consecutive decode steps per request.  ``x`` and ``out`` are ``[bs, T, H, P]``;
     ``dt`` is ``[bs, T, H]`` (or ``[bs, T, H, P]`` with stride 0 over P); ``B`` and ``C`` are
-    ``[bs, T, G, N]``; ``intermediate`` (optional, fp32 ``[bs, T, H, P, N]``) receives the
-    state after every token.  Per-head operands as for ``ssu_update``."""
+    ``[bs, T, G, N]``; ``intermediate`` (optional, ``[bs, T, H, P, N]`` of the state's dtype)
+    receives the state after every token.  Per-head operands as for ``ssu_update``."""
     for name, t, nd in (("x", x, 4), ("out", out, 4), ("B", B, 4), ("C", C, 4)):
         if not isinstance(t, torch.Tensor) or t.dim() != nd:
             raise ValueError(f"{name} must be a {nd}-D tensor with a token dimension")
@@ -340,7 +346,7 @@ def ssu_update_tokens(handle: int, state_pool, state_batch_indices, x, dt, dt_bi
     ts.x, ts.out, ts.dt, ts.B, ts.C = (x.stride(1), out.stride(1), dt.stride(1), B.stride(1),
                                        C.stride(1))
     if intermediate is not None:
-        _expect(intermediate, "intermediate", torch.float32, (5,))
+        _expect(intermediate, "intermediate", state_pool.dtype, (5,))
         if tuple(intermediate.shape) != (x.shape[0], T, x.shape[2], x.shape[3],
                                          state_pool.shape[3]):
             raise ValueError("intermediate must be [bs, T, H, P, N]")

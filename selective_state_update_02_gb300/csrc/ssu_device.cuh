@@ -10,8 +10,8 @@
 
 namespace {
 
-constexpr int kDstate = 128;             // dstate this build implements: 32 lanes x 4 columns
-constexpr int kRowBytes = kDstate * 4;   // one fp32 state row
+constexpr int kDstate = 128;             // dstate of the BULK kernel: 32 lanes x 4 columns
+constexpr int kRowBytes = kDstate * 4;   // one fp32 state row of the BULK kernel
 constexpr int kMaxWarpsPerCta = 16;      // VEC
 constexpr int kMaxBulkWarps = 8;         // BULK compute warps (plus one producer warp)
 constexpr int kMaxStages = 8;
@@ -19,7 +19,7 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per mbarrier 
 
 // Everything one launch needs, passed by value in the kernel parameter space.
 struct SsuParams {
-    float *state;
+    void *state;  // fp32 or bf16 elements (the kernel's template parameter says which)
     const void *idx;
     const __nv_bfloat16 *x;
     const __nv_bfloat16 *dt;
@@ -62,6 +62,101 @@ __device__ __forceinline__ float update_cols(float4 &w, float dA, float k, const
     part = fmaf(w.y, cc[1], part);
     part = fmaf(w.z, cc[2], part);
     part = fmaf(w.w, cc[3], part);
+    return part;
+}
+
+// ---------------------------------------------------------------------------------------
+// Columns of a row owned by one lane, for dstate N = 32 * NC (NC = 2, 4 or 8).  With NC = 2
+// lane l owns columns 2l, 2l+1; with NC = 4 columns 4l..4l+3; with NC = 8 the two groups
+// 4l..4l+3 and 128+4l..128+4l+3, so every vector instruction of a warp covers one contiguous
+// span of the row.  The lane's j-th value is column col_of<NC>(lane, j).
+
+template <int NC>
+__device__ __forceinline__ int col_of(int lane, int j) {
+    if (NC == 2) return 2 * lane + j;
+    return (j / 4) * 128 + 4 * lane + (j % 4);
+}
+
+__device__ __forceinline__ float2 bf2_to_f2(unsigned bits) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bits));
+}
+
+__device__ __forceinline__ unsigned f2_to_bf2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // round to nearest even
+    return *reinterpret_cast<const unsigned *>(&h);
+}
+
+// Streaming (evict-first) load of one lane's NC columns of a row, widened to fp32.
+template <int NC, typename ST>
+__device__ __forceinline__ void load_cols(const ST *row, int lane, float (&v)[NC]) {
+    if constexpr (sizeof(ST) == 4) {
+        if constexpr (NC == 2) {
+            const float2 a = __ldcs(reinterpret_cast<const float2 *>(row) + lane);
+            v[0] = a.x, v[1] = a.y;
+        } else {
+#pragma unroll
+            for (int g = 0; g < NC / 4; ++g) {
+                const float4 a = __ldcs(reinterpret_cast<const float4 *>(row + g * 128) + lane);
+                v[4 * g] = a.x, v[4 * g + 1] = a.y, v[4 * g + 2] = a.z, v[4 * g + 3] = a.w;
+            }
+        }
+    } else {
+        if constexpr (NC == 2) {
+            const float2 a = bf2_to_f2(__ldcs(reinterpret_cast<const unsigned *>(row) + lane));
+            v[0] = a.x, v[1] = a.y;
+        } else {
+#pragma unroll
+            for (int g = 0; g < NC / 4; ++g) {
+                const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(row + g * 128) + lane);
+                const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y);
+                v[4 * g] = a.x, v[4 * g + 1] = a.y, v[4 * g + 2] = b.x, v[4 * g + 3] = b.y;
+            }
+        }
+    }
+}
+
+// Streaming store of one lane's NC columns (rounded to bf16, nearest even, for a bf16 state).
+template <int NC, typename ST>
+__device__ __forceinline__ void store_cols(ST *row, int lane, const float (&v)[NC]) {
+    if constexpr (sizeof(ST) == 4) {
+        if constexpr (NC == 2) {
+            __stcs(reinterpret_cast<float2 *>(row) + lane, make_float2(v[0], v[1]));
+        } else {
+#pragma unroll
+            for (int g = 0; g < NC / 4; ++g)
+                __stcs(reinterpret_cast<float4 *>(row + g * 128) + lane,
+                       make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
+        }
+    } else {
+        if constexpr (NC == 2) {
+            __stcs(reinterpret_cast<unsigned *>(row) + lane, f2_to_bf2(v[0], v[1]));
+        } else {
+#pragma unroll
+            for (int g = 0; g < NC / 4; ++g)
+                __stcs(reinterpret_cast<uint2 *>(row + g * 128) + lane,
+                       make_uint2(f2_to_bf2(v[4 * g], v[4 * g + 1]),
+                                  f2_to_bf2(v[4 * g + 2], v[4 * g + 3])));
+        }
+    }
+}
+
+// The lane's NC columns of B (or C) for group g of request b, widened to fp32.
+template <int NC>
+__device__ __forceinline__ void load_bc(const __nv_bfloat16 *base, int lane, float (&o)[NC]) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) o[j] = __bfloat162float(base[col_of<NC>(lane, j)]);
+}
+
+// The update of one lane's NC columns of one row; returns the lane's part of the readout
+// (its columns summed in order j = 0, 1, ...); for NC = 4 the same operations as update_cols.
+template <int NC>
+__device__ __forceinline__ float update_lane(float (&v)[NC], float dA, float k,
+                                             const float (&bb)[NC], const float (&cc)[NC]) {
+#pragma unroll
+    for (int j = 0; j < NC; ++j) v[j] = fmaf(v[j], dA, k * bb[j]);
+    float part = v[0] * cc[0];
+#pragma unroll
+    for (int j = 1; j < NC; ++j) part = fmaf(v[j], cc[j], part);
     return part;
 }
 

@@ -9,7 +9,6 @@
 
 namespace ssu_host {
 
-constexpr int kDstate = 128;  // dstate this build implements
 
 namespace {
 thread_local std::string g_last_error;
@@ -34,7 +33,7 @@ bool aligned(const void *ptr, unsigned bytes) {
     return (reinterpret_cast<unsigned long long>(ptr) % bytes) == 0;
 }
 
-ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint16_t *x,
+ssu_status_t validate_impl(const void *state_pool, const void *idx, const uint16_t *x,
                            const uint16_t *dt, const float *dt_bias, const float *A,
                            const uint16_t *B, const uint16_t *C, const float *D,
                            const uint16_t *out, const ssu_shape_t *shape,
@@ -50,8 +49,10 @@ ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint1
                     (long long)s.nheads, (long long)s.ngroups);
     if (s.index_dtype != SSU_INDEX_I32 && s.index_dtype != SSU_INDEX_I64)
         return fail(SSU_ERR_INVALID_ARG, "index_dtype %d is neither I32 nor I64", s.index_dtype);
-    if (s.dstate != kDstate)
-        return fail(SSU_ERR_UNSUPPORTED, "dstate %lld: this build implements dstate 128",
+    if (s.state_dtype != SSU_STATE_F32 && s.state_dtype != SSU_STATE_BF16)
+        return fail(SSU_ERR_INVALID_ARG, "state_dtype %d is neither F32 nor BF16", s.state_dtype);
+    if (s.dstate != 64 && s.dstate != 128 && s.dstate != 256)
+        return fail(SSU_ERR_UNSUPPORTED, "dstate %lld: this build implements 64, 128 and 256",
                     (long long)s.dstate);
     if (s.headdim > (1 << 20) || s.nheads > (1 << 20))
         return fail(SSU_ERR_UNSUPPORTED, "headdim and nheads are limited to 2^20");
@@ -74,10 +75,12 @@ ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint1
         return fail(SSU_ERR_UNSUPPORTED, "dt_bias and D must be constant over headdim");
     if (st->A[1] != 0 || st->A[2] != 0)
         return fail(SSU_ERR_UNSUPPORTED, "A must be constant over headdim and dstate");
+    const int per16 = s.state_dtype == SSU_STATE_BF16 ? 8 : 4;  // elements per 16 bytes
     for (int j = 0; j < 3; ++j)
-        if (st->state[j] % 4 != 0)
-            return fail(SSU_ERR_MISALIGNED, "state stride %d (%lld) is not a multiple of 4 floats",
-                        j, (long long)st->state[j]);
+        if (st->state[j] % per16 != 0)
+            return fail(SSU_ERR_MISALIGNED,
+                        "state stride %d (%lld elements) is not a multiple of 16 bytes", j,
+                        (long long)st->state[j]);
 
     if (!state_pool || !idx || !x || !dt || !dt_bias || !A || !B || !C || !D || !out)
         return fail(SSU_ERR_INVALID_ARG, "a data pointer is NULL");

@@ -16,7 +16,7 @@ ssu_status_t fail(ssu_status_t status, const char *fmt, ...);
 ssu_status_t ok();
 bool aligned(const void *ptr, unsigned bytes);
 // The full host-side validation of one ssu_update / ssu_update_static call.
-ssu_status_t validate_impl(const float *state_pool, const void *idx, const uint16_t *x,
+ssu_status_t validate_impl(const void *state_pool, const void *idx, const uint16_t *x,
                            const uint16_t *dt, const float *dt_bias, const float *A,
                            const uint16_t *B, const uint16_t *C, const float *D,
                            const uint16_t *out, const ssu_shape_t *shape,

@@ -1,10 +1,11 @@
 // Multi-token decode step for GB300 (sm_103a): T consecutive tokens of every request in one
 // call (the verification step of multi-token speculation, vLLM PR #48110, Test Plan).  Token t
 // applies the single-token update to the state token t - 1 left; the state is loaded once,
-// kept in registers across the T tokens, and stored once.  The element mapping, update order
-// and readout tree are those of the single-token VEC kernel (ssu_device.cuh), so T = 1
-// reproduces ssu_update bit for bit.  Each warp prefetches token t + 1's inputs (dt, its 4
-// columns of B and C, one x row per lane) while it updates token t.
+// kept in registers (fp32) across the T tokens, and stored once.  Templated like the VEC
+// kernel (rows per warp, columns per lane with dstate = 32 * NC, state type, index type), with
+// its element mapping, update order and readout tree, so T = 1 reproduces ssu_update bit for
+// bit.  Each warp prefetches token t + 1's inputs (dt, its NC columns of B and C, one x row per
+// lane) while it updates token t.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -26,39 +27,35 @@ namespace {
 
 struct TokenParams {
     SsuParams p;
-    float *inter;                      // optional intermediate states, may be null
+    void *inter;                       // optional intermediate states (state dtype), may be null
     long long x_t, out_t, dt_t, B_t, C_t;
     long long in_b, in_t, in_h, in_p;  // intermediate strides; dstate stride is 1
     int tokens;
 };
 
 // One token's inputs for one warp: lane r < RPW holds x of row r.
+template <int NC>
 struct TokenIn {
     float dt;
-    float bb[4], cc[4];
+    float bb[NC], cc[NC];
     float x;
 };
 
-template <int RPW>
-__device__ __forceinline__ TokenIn load_token(const TokenParams &q, long long b, int h, int g,
-                                              int row0, int t, int lane) {
+template <int RPW, int NC>
+__device__ __forceinline__ TokenIn<NC> load_token(const TokenParams &q, long long b, int h,
+                                                  int g, int row0, int t, int lane) {
     const SsuParams &p = q.p;
-    TokenIn in;
+    TokenIn<NC> in;
     in.dt = __bfloat162float(p.dt[b * p.dt_b + t * q.dt_t + h * p.dt_h]);
-    const __nv_bfloat16 *Bp = p.B + b * p.B_b + t * q.B_t + g * p.B_g + lane * 4;
-    const __nv_bfloat16 *Cp = p.C + b * p.C_b + t * q.C_t + g * p.C_g + lane * 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        in.bb[j] = __bfloat162float(Bp[j]);
-        in.cc[j] = __bfloat162float(Cp[j]);
-    }
+    load_bc<NC>(p.B + b * p.B_b + t * q.B_t + g * p.B_g, lane, in.bb);
+    load_bc<NC>(p.C + b * p.C_b + t * q.C_t + g * p.C_g, lane, in.cc);
     in.x = (lane < RPW && row0 + lane < p.headdim)
                ? __bfloat162float(p.x[b * p.x_b + t * q.x_t + h * p.x_h + row0 + lane])
                : 0.f;
     return in;
 }
 
-template <int RPW, bool kIdx64>
+template <int RPW, int NC, typename ST, bool kIdx64>
 __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     ssu_tokens_kernel(const __grid_constant__ TokenParams q) {
     const SsuParams &p = q.p;
@@ -76,36 +73,41 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         return;
     }
     const int row0 = slab * p.rows_per_cta + warp * RPW;
-    float *srow = p.state + s * p.st_pool + h * p.st_head + row0 * p.st_row + lane * 4;
+    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row;
 
-    float4 v[RPW];
+    float v[RPW][NC];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
-        v[r] = row0 + r < p.headdim ? __ldcs(reinterpret_cast<const float4 *>(srow + r * p.st_row))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < RPW; ++r) {
+        if (row0 + r < p.headdim) {
+            load_cols<NC, ST>(srow + r * p.st_row, lane, v[r]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
+        }
+    }
 
     const float bias = p.dt_bias[h * p.bias_h];
     const float Ah = p.A[h * p.A_h];
     const float Dh = p.D[h * p.D_h];
     const int g = h / p.heads_per_group;
-    TokenIn cur = load_token<RPW>(q, b, h, g, row0, 0, lane);
+    TokenIn<NC> cur = load_token<RPW, NC>(q, b, h, g, row0, 0, lane);
     for (int t = 0; t < q.tokens; ++t) {
-        TokenIn nxt = cur;
-        if (t + 1 < q.tokens) nxt = load_token<RPW>(q, b, h, g, row0, t + 1, lane);
+        TokenIn<NC> nxt = cur;
+        if (t + 1 < q.tokens) nxt = load_token<RPW, NC>(q, b, h, g, row0, t + 1, lane);
         const float dtv = softplus_f32(cur.dt + bias);
         const float dA = expf(dtv * Ah);
         float part[RPW];
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const float xr = __shfl_sync(0xffffffffu, cur.x, r);
-            part[r] = update_cols(v[r], dA, dtv * xr, cur.bb, cur.cc);
+            part[r] = update_lane<NC>(v[r], dA, dtv * xr, cur.bb, cur.cc);
         }
         if (q.inter) {
-            float *irow = q.inter + b * q.in_b + t * q.in_t + h * q.in_h + row0 * q.in_p + lane * 4;
+            ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
+                       row0 * q.in_p;
 #pragma unroll
             for (int r = 0; r < RPW; ++r)
-                if (row0 + r < p.headdim)
-                    __stcs(reinterpret_cast<float4 *>(irow + r * q.in_p), v[r]);
+                if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, lane, v[r]);
         }
         const float total = reduce_rows<RPW>(part, lane);
         const int rl = row_of_lane<RPW>(lane);
@@ -117,30 +119,47 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     }
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
-        if (row0 + r < p.headdim) __stcs(reinterpret_cast<float4 *>(srow + r * p.st_row), v[r]);
+        if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, lane, v[r]);
 }
 
-template <bool kIdx64>
-cudaError_t launch_tokens(const TokenParams &q, int rpw, int wpc, unsigned grid,
-                          cudaStream_t st) {
+template <int NC, typename ST, bool kIdx64>
+cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, unsigned grid,
+                            cudaStream_t st) {
     const dim3 block(32 * wpc);
     switch (rpw) {
-        case 1: ssu_tokens_kernel<1, kIdx64><<<grid, block, 0, st>>>(q); break;
-        case 2: ssu_tokens_kernel<2, kIdx64><<<grid, block, 0, st>>>(q); break;
-        case 4: ssu_tokens_kernel<4, kIdx64><<<grid, block, 0, st>>>(q); break;
-        case 8: ssu_tokens_kernel<8, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 1: ssu_tokens_kernel<1, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 2: ssu_tokens_kernel<2, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 4: ssu_tokens_kernel<4, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 8: ssu_tokens_kernel<8, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
+cudaError_t launch_tokens(const TokenParams &q, int nc, bool bf16, bool i64, int rpw, int wpc,
+                          unsigned grid, cudaStream_t st) {
+#define SSU_TOK_NC(NC_)                                                                      \
+    if (nc == NC_) {                                                                         \
+        if (bf16)                                                                            \
+            return i64 ? launch_tokens_t<NC_, __nv_bfloat16, true>(q, rpw, wpc, grid, st)    \
+                       : launch_tokens_t<NC_, __nv_bfloat16, false>(q, rpw, wpc, grid, st);  \
+        return i64 ? launch_tokens_t<NC_, float, true>(q, rpw, wpc, grid, st)                \
+                   : launch_tokens_t<NC_, float, false>(q, rpw, wpc, grid, st);              \
+    }
+    SSU_TOK_NC(2)
+    SSU_TOK_NC(4)
+    SSU_TOK_NC(8)
+#undef SSU_TOK_NC
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, float *state_pool,
+extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                                           const void *state_batch_indices, const uint16_t *x,
                                           const uint16_t *dt, const float *dt_bias,
                                           const float *A, const uint16_t *B, const uint16_t *C,
-                                          const float *D, uint16_t *out, float *intermediate,
+                                          const float *D, uint16_t *out, void *intermediate,
                                           const ssu_shape_t *shape, const ssu_strides_t *strides,
                                           int64_t tokens, const ssu_token_strides_t *ts,
                                           ssu_stream_t stream) {
@@ -159,9 +178,11 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, float *state_pool
             if (ts->intermediate[j] < 0) return fail(SSU_ERR_INVALID_ARG, "negative stride");
         if (ts->intermediate[4] != 1)
             return fail(SSU_ERR_UNSUPPORTED, "intermediate dstate-stride must be 1");
+        const int per16 = shape->state_dtype == SSU_STATE_BF16 ? 8 : 4;
         for (int j = 0; j < 4; ++j)
-            if (ts->intermediate[j] % 4)
-                return fail(SSU_ERR_MISALIGNED, "intermediate strides must be multiples of 4");
+            if (ts->intermediate[j] % per16)
+                return fail(SSU_ERR_MISALIGNED,
+                            "intermediate strides must be multiples of 16 bytes");
         if (!aligned(intermediate, 16))
             return fail(SSU_ERR_MISALIGNED, "intermediate is not 16-byte aligned");
     }
@@ -228,10 +249,10 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, float *state_pool
     if (guard.err != cudaSuccess)
         return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e =
-        s.index_dtype == SSU_INDEX_I64
-            ? launch_tokens<true>(q, rpw, wpc, static_cast<unsigned>(tiles), cs)
-            : launch_tokens<false>(q, rpw, wpc, static_cast<unsigned>(tiles), cs);
+    const cudaError_t e = launch_tokens(q, static_cast<int>(s.dstate / 32),
+                                        s.state_dtype == SSU_STATE_BF16,
+                                        s.index_dtype == SSU_INDEX_I64, rpw, wpc,
+                                        static_cast<unsigned>(tiles), cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }

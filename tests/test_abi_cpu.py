@@ -108,7 +108,8 @@ def test_empty_batch_needs_no_pointers(ssu):
     (lambda p, s, t: setattr(s, "batch", -1), "INVALID_ARG"),
     (lambda p, s, t: setattr(s, "ngroups", 3), "INVALID_ARG"),           # 16 % 3 != 0
     (lambda p, s, t: setattr(s, "index_dtype", 7), "INVALID_ARG"),
-    (lambda p, s, t: setattr(s, "dstate", 64), "UNSUPPORTED"),
+    (lambda p, s, t: setattr(s, "dstate", 96), "UNSUPPORTED"),
+    (lambda p, s, t: setattr(s, "state_dtype", 5), "INVALID_ARG"),
     (lambda p, s, t: t.state.__setitem__(3, 2), "UNSUPPORTED"),
     (lambda p, s, t: t.state.__setitem__(2, 130), "MISALIGNED"),
     (lambda p, s, t: p.__setitem__(0, BASE + 4), "MISALIGNED"),
@@ -125,6 +126,18 @@ def test_invalid_calls_return_their_code(ssu, mutate, code):
     mutate(ptrs, shape, st)
     assert validate(ssu, ptrs, shape, st) == getattr(ssu, "SSU_ERR_" + code)
     assert ssu.last_error() != ""
+
+
+def test_other_dstate_buckets_and_bf16_state(ssu):
+    for N in (64, 256):
+        assert validate(ssu, *canonical(N=N)) == ssu.SSU_OK
+    ptrs, shape, st = canonical()
+    shape.state_dtype = ssu.SSU_STATE_BF16
+    assert validate(ssu, ptrs, shape, st) == ssu.SSU_OK
+    st.state[2] = 132            # 264 bytes: not a multiple of 16 for bf16 rows
+    assert validate(ssu, ptrs, shape, st) == ssu.SSU_ERR_MISALIGNED
+    shape.state_dtype = ssu.SSU_STATE_F32
+    assert validate(ssu, ptrs, shape, st) == ssu.SSU_OK   # 528 bytes for fp32
 
 
 def test_i64_indices_must_be_8_byte_aligned(ssu):

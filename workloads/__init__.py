@@ -43,7 +43,7 @@ def bf16_bits_to_f32(bits) -> np.ndarray:
 class Problem:
     """One decode-step problem in host memory (bf16 operands held as uint16 patterns)."""
 
-    pool: np.ndarray      # float32 [pool_size, H, P, N]
+    pool: np.ndarray      # float32 [pool_size, H, P, N], or uint16 bf16 patterns
     idx: np.ndarray       # int64 [bs] (or [n_sets, bs] for rotation sets)
     x: np.ndarray         # uint16 [bs, H, P]
     dt: np.ndarray        # uint16 [bs, H]
@@ -87,13 +87,15 @@ def request_inputs(rng: np.random.Generator, bs: int, H: int, P: int = HEADDIM,
 
 
 def state_pool(rng: np.random.Generator, pool_size: int, H: int, P: int = HEADDIM,
-               N: int = DSTATE) -> np.ndarray:
-    """fp32 state pool ~ N(0, 1)."""
-    return rng.standard_normal((pool_size, H, P, N), dtype=np.float32)
+               N: int = DSTATE, dtype: str = "f32") -> np.ndarray:
+    """State pool ~ N(0, 1): fp32 values, or (dtype "bf16") the same draws rounded to bf16
+    patterns (uint16)."""
+    pool = rng.standard_normal((pool_size, H, P, N), dtype=np.float32)
+    return f32_to_bf16_bits(pool) if dtype == "bf16" else pool
 
 
 def make_problem(bs: int, H: int = 16, P: int = HEADDIM, N: int = DSTATE, G: int = 1,
-                 pool_size: int | None = None, seed: int = 0) -> Problem:
+                 pool_size: int | None = None, seed: int = 0, state_dtype: str = "f32") -> Problem:
     """A problem whose ``idx`` is ``bs`` distinct slots drawn at random from the pool.
 
     The tiny parity workload is ``make_problem(8, 16, pool_size=32, seed=0)``: batch 8,
@@ -104,7 +106,7 @@ def make_problem(bs: int, H: int = 16, P: int = HEADDIM, N: int = DSTATE, G: int
     if pool_size < bs:
         raise ValueError("pool must hold at least one slot per request")
     rng = np.random.default_rng(seed)
-    pool = state_pool(rng, pool_size, H, P, N)
+    pool = state_pool(rng, pool_size, H, P, N, state_dtype)
     idx = rng.permutation(pool_size)[:bs].astype(np.int64)
     dt_bias, A, D = head_params(rng, H)
     x, dt, B, C = request_inputs(rng, bs, H, P, N, G)
@@ -123,13 +125,14 @@ def rotation_sets(bs: int, n_sets: int, seed: int = 0) -> np.ndarray:
 
 
 def sets_for_cold_l2(bs: int, H: int, l2_bytes: int, factor: float = 3.0,
-                     P: int = HEADDIM, N: int = DSTATE, min_sets: int = 3) -> int:
+                     P: int = HEADDIM, N: int = DSTATE, min_sets: int = 3,
+                     elem_bytes: int = 4) -> int:
     """Number of disjoint slot sets whose states together hold ``factor`` x the L2 size.
 
     Mirrors the cold-L2 rotation of sglang PR #41223 (Details / Kernel measurement): call i of
     a timed sequence touches set (i mod K), and the K sets hold at least 3x the L2.
     """
-    set_bytes = bs * H * P * N * 4
+    set_bytes = bs * H * P * N * elem_bytes
     return max(min_sets, math.ceil(factor * l2_bytes / set_bytes))
 
 
