@@ -342,9 +342,28 @@ def time_e2e(wl_, handle, steps: int, dev) -> dict:
         ev1.record(stream)
     stream.synchronize()
     ms = ev0.elapsed_time(ev1)
+    # The same calls captured once in a CUDA graph (copies from and to the same pinned host
+    # buffers are graph nodes), as a serving loop that replays its decode step would run them.
+    g = torch.cuda.CUDAGraph()
+    per_graph = wl_.n_sets * max(1, math.ceil(100 / wl_.n_sets))
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(per_graph):
+            step(i % wl_.n_sets)
+    g.replay()
+    stream.synchronize()
+    reps = max(1, steps // per_graph)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    graph_us = ev0.elapsed_time(ev1) * 1000.0 / (reps * per_graph)
     return {"value": round(ms * 1000.0 / steps, 3), "unit": UNIT, "steps": steps,
             "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": bs * H * HEADDIM * 2,
-            "path": "binding ssu_update (C ABI) per step, pinned host buffers, eager"}
+            "path": "binding ssu_update (C ABI) per step, pinned host buffers, eager",
+            "graph_value": round(graph_us, 3),
+            "graph_path": "the same per-step copies and ssu_update captured in a CUDA graph"}
 
 
 # ---- the oracle on the host cores -----------------------------------------------------------

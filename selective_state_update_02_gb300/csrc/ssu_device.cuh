@@ -69,12 +69,14 @@ __device__ __forceinline__ float update_cols(float4 &w, float dA, float k, const
 // Columns of a row owned by one lane, for dstate N = 32 * NC (NC = 2, 4 or 8).  With NC = 2
 // lane l owns columns 2l, 2l+1; with NC = 4 columns 4l..4l+3; with NC = 8 the two groups
 // 4l..4l+3 and 128+4l..128+4l+3, so every vector instruction of a warp covers one contiguous
-// span of the row.  The lane's j-th value is column col_of<NC>(lane, j).
+// span of the row.  The lane's j-th value is column lane_offset<NC>(lane) + (j / 4) * 128 +
+// j % 4.
 
+// Offset of a lane's first column in a row (its columns then sit at +0..3 and, for NC = 8,
+// +128..131; for NC = 2 at +0..1).  Kernels add it to the row pointer once.
 template <int NC>
-__device__ __forceinline__ int col_of(int lane, int j) {
-    if (NC == 2) return 2 * lane + j;
-    return (j / 4) * 128 + 4 * lane + (j % 4);
+__device__ __forceinline__ int lane_offset(int lane) {
+    return NC == 2 ? 2 * lane : 4 * lane;
 }
 
 __device__ __forceinline__ float2 bf2_to_f2(unsigned bits) {
@@ -86,28 +88,29 @@ __device__ __forceinline__ unsigned f2_to_bf2(float a, float b) {
     return *reinterpret_cast<const unsigned *>(&h);
 }
 
-// Streaming (evict-first) load of one lane's NC columns of a row, widened to fp32.
+// Streaming (evict-first) load of one lane's NC columns of a row, widened to fp32.  `p` points
+// at the lane's first column (row + lane_offset<NC>(lane)).
 template <int NC, typename ST>
-__device__ __forceinline__ void load_cols(const ST *row, int lane, float (&v)[NC]) {
+__device__ __forceinline__ void load_cols(const ST *p, float (&v)[NC]) {
     if constexpr (sizeof(ST) == 4) {
         if constexpr (NC == 2) {
-            const float2 a = __ldcs(reinterpret_cast<const float2 *>(row) + lane);
+            const float2 a = __ldcs(reinterpret_cast<const float2 *>(p));
             v[0] = a.x, v[1] = a.y;
         } else {
 #pragma unroll
             for (int g = 0; g < NC / 4; ++g) {
-                const float4 a = __ldcs(reinterpret_cast<const float4 *>(row + g * 128) + lane);
+                const float4 a = __ldcs(reinterpret_cast<const float4 *>(p + g * 128));
                 v[4 * g] = a.x, v[4 * g + 1] = a.y, v[4 * g + 2] = a.z, v[4 * g + 3] = a.w;
             }
         }
     } else {
         if constexpr (NC == 2) {
-            const float2 a = bf2_to_f2(__ldcs(reinterpret_cast<const unsigned *>(row) + lane));
+            const float2 a = bf2_to_f2(__ldcs(reinterpret_cast<const unsigned *>(p)));
             v[0] = a.x, v[1] = a.y;
         } else {
 #pragma unroll
             for (int g = 0; g < NC / 4; ++g) {
-                const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(row + g * 128) + lane);
+                const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p + g * 128));
                 const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y);
                 v[4 * g] = a.x, v[4 * g + 1] = a.y, v[4 * g + 2] = b.x, v[4 * g + 3] = b.y;
             }
@@ -115,36 +118,37 @@ __device__ __forceinline__ void load_cols(const ST *row, int lane, float (&v)[NC
     }
 }
 
-// Streaming store of one lane's NC columns (rounded to bf16, nearest even, for a bf16 state).
+// Streaming store of one lane's NC columns (rounded to bf16, nearest even, for a bf16 state);
+// `p` points at the lane's first column.
 template <int NC, typename ST>
-__device__ __forceinline__ void store_cols(ST *row, int lane, const float (&v)[NC]) {
+__device__ __forceinline__ void store_cols(ST *p, const float (&v)[NC]) {
     if constexpr (sizeof(ST) == 4) {
         if constexpr (NC == 2) {
-            __stcs(reinterpret_cast<float2 *>(row) + lane, make_float2(v[0], v[1]));
+            __stcs(reinterpret_cast<float2 *>(p), make_float2(v[0], v[1]));
         } else {
 #pragma unroll
             for (int g = 0; g < NC / 4; ++g)
-                __stcs(reinterpret_cast<float4 *>(row + g * 128) + lane,
+                __stcs(reinterpret_cast<float4 *>(p + g * 128),
                        make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
         }
     } else {
         if constexpr (NC == 2) {
-            __stcs(reinterpret_cast<unsigned *>(row) + lane, f2_to_bf2(v[0], v[1]));
+            __stcs(reinterpret_cast<unsigned *>(p), f2_to_bf2(v[0], v[1]));
         } else {
 #pragma unroll
             for (int g = 0; g < NC / 4; ++g)
-                __stcs(reinterpret_cast<uint2 *>(row + g * 128) + lane,
+                __stcs(reinterpret_cast<uint2 *>(p + g * 128),
                        make_uint2(f2_to_bf2(v[4 * g], v[4 * g + 1]),
                                   f2_to_bf2(v[4 * g + 2], v[4 * g + 3])));
         }
     }
 }
 
-// The lane's NC columns of B (or C) for group g of request b, widened to fp32.
+// The lane's NC columns of B (or C), widened to fp32; `p` points at the lane's first column.
 template <int NC>
-__device__ __forceinline__ void load_bc(const __nv_bfloat16 *base, int lane, float (&o)[NC]) {
+__device__ __forceinline__ void load_bc(const __nv_bfloat16 *p, float (&o)[NC]) {
 #pragma unroll
-    for (int j = 0; j < NC; ++j) o[j] = __bfloat162float(base[col_of<NC>(lane, j)]);
+    for (int j = 0; j < NC; ++j) o[j] = __bfloat162float(p[(j / 4) * 128 + (j % 4)]);
 }
 
 // The update of one lane's NC columns of one row; returns the lane's part of the readout

@@ -47,8 +47,8 @@ __device__ __forceinline__ TokenIn<NC> load_token(const TokenParams &q, long lon
     const SsuParams &p = q.p;
     TokenIn<NC> in;
     in.dt = __bfloat162float(p.dt[b * p.dt_b + t * q.dt_t + h * p.dt_h]);
-    load_bc<NC>(p.B + b * p.B_b + t * q.B_t + g * p.B_g, lane, in.bb);
-    load_bc<NC>(p.C + b * p.C_b + t * q.C_t + g * p.C_g, lane, in.cc);
+    load_bc<NC>(p.B + b * p.B_b + t * q.B_t + g * p.B_g + lane_offset<NC>(lane), in.bb);
+    load_bc<NC>(p.C + b * p.C_b + t * q.C_t + g * p.C_g + lane_offset<NC>(lane), in.cc);
     in.x = (lane < RPW && row0 + lane < p.headdim)
                ? __bfloat162float(p.x[b * p.x_b + t * q.x_t + h * p.x_h + row0 + lane])
                : 0.f;
@@ -73,13 +73,14 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         return;
     }
     const int row0 = slab * p.rows_per_cta + warp * RPW;
-    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row;
+    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row +
+               lane_offset<NC>(lane);
 
     float v[RPW][NC];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         if (row0 + r < p.headdim) {
-            load_cols<NC, ST>(srow + r * p.st_row, lane, v[r]);
+            load_cols<NC, ST>(srow + r * p.st_row, v[r]);
         } else {
 #pragma unroll
             for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
@@ -104,10 +105,10 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         }
         if (q.inter) {
             ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
-                       row0 * q.in_p;
+                       row0 * q.in_p + lane_offset<NC>(lane);
 #pragma unroll
             for (int r = 0; r < RPW; ++r)
-                if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, lane, v[r]);
+                if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, v[r]);
         }
         const float total = reduce_rows<RPW>(part, lane);
         const int rl = row_of_lane<RPW>(lane);
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     }
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
-        if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, lane, v[r]);
+        if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
 }
 
 template <int NC, typename ST, bool kIdx64>

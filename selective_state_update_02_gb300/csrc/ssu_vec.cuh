@@ -27,14 +27,15 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     }
 
     const int row0 = slab * p.rows_per_cta + warp * RPW;
-    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row;
+    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row +
+               lane_offset<NC>(lane);
 
     // Issue every state load of this warp before anything that depends on other loads.
     float v[RPW][NC];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         if (row0 + r < p.headdim) {
-            load_cols<NC, ST>(srow + r * p.st_row, lane, v[r]);
+            load_cols<NC, ST>(srow + r * p.st_row, v[r]);
         } else {
 #pragma unroll
             for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
@@ -48,8 +49,8 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     const float Dh = p.D[h * p.D_h];
     const int g = h / p.heads_per_group;
     float bb[NC], cc[NC];
-    load_bc<NC>(p.B + b * p.B_b + g * p.B_g, lane, bb);
-    load_bc<NC>(p.C + b * p.C_b + g * p.C_g, lane, cc);
+    load_bc<NC>(p.B + b * p.B_b + g * p.B_g + lane_offset<NC>(lane), bb);
+    load_bc<NC>(p.C + b * p.C_b + g * p.C_g + lane_offset<NC>(lane), cc);
     const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
 
     float part[RPW];
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         const bool live = row0 + r < p.headdim;
         const float xr = live ? __bfloat162float(xp[r]) : 0.f;
         part[r] = update_lane<NC>(v[r], dA, dtv * xr, bb, cc);
-        if (live) store_cols<NC, ST>(srow + r * p.st_row, lane, v[r]);
+        if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
     }
     const float total = reduce_rows<RPW>(part, lane);
     const int rl = row_of_lane<RPW>(lane);
