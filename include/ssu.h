@@ -69,7 +69,7 @@ typedef enum { SSU_STATE_F32 = 0, SSU_STATE_BF16 = 1 } ssu_state_dtype_t;
 /* Problem sizes of one call. */
 typedef struct {
     int64_t batch;       /* bs: requests in this step; 0 is valid and enqueues nothing */
-    int64_t nheads;      /* H >= 1 */
+    int64_t nheads;      /* H: 1..65535 */
     int64_t headdim;     /* P >= 1 */
     int64_t dstate;      /* N: 64, 128 or 256 */
     int64_t ngroups;     /* G >= 1 with H % G == 0; head h reads group h / (H / G) */

@@ -235,6 +235,7 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
     p.A_h = strides->A[0];
     p.idx_s = strides->idx;
     p.pool_size = s.pool_size;
+    p.batch = s.batch;
     p.nheads = static_cast<int>(s.nheads);
     p.headdim = static_cast<int>(s.headdim);
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
@@ -263,8 +264,10 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
             e = cudaGetLastError();
         }
     } else {
+        const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
+                        static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
         e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16, i64,
-                       l.rows_per_warp, l.warps_per_cta, static_cast<unsigned>(tiles), cs);
+                       l.rows_per_warp, l.warps_per_cta, grid, cs);
     }
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
@@ -395,6 +398,7 @@ extern "C" ssu_status_t ssu_update_static(void *state_pool, const void *state_ba
     p.A_h = strides->A[0];
     p.idx_s = strides->idx;
     p.pool_size = s.pool_size;
+    p.batch = s.batch;
     p.nheads = static_cast<int>(s.nheads);
     p.headdim = static_cast<int>(s.headdim);
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
@@ -409,7 +413,9 @@ extern "C" ssu_status_t ssu_update_static(void *state_pool, const void *state_ba
     if (e == cudaSuccess)
         e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16,
                        s.index_dtype == SSU_INDEX_I64, l.rows_per_warp, l.warps_per_cta,
-                       static_cast<unsigned>(tiles), cs);
+                       dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
+                            static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535)),
+                       cs);
     if (e == cudaSuccess && counters_out)
         e = cudaMemcpyAsync(counters_out, scratch, 3 * sizeof(unsigned),
                             cudaMemcpyDeviceToDevice, cs);

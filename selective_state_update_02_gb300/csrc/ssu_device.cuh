@@ -34,6 +34,7 @@ struct SsuParams {
     long long B_b, B_g, C_b, C_g;
     long long bias_h, D_h, A_h, idx_s;
     long long pool_size;
+    long long batch;
     int nheads, headdim, heads_per_group;
     int slabs;         // tiles per (request, head) unit
     int rows_per_cta;  // rows per tile

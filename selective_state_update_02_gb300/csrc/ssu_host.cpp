@@ -54,8 +54,8 @@ ssu_status_t validate_impl(const void *state_pool, const void *idx, const uint16
     if (s.dstate != 64 && s.dstate != 128 && s.dstate != 256)
         return fail(SSU_ERR_UNSUPPORTED, "dstate %lld: this build implements 64, 128 and 256",
                     (long long)s.dstate);
-    if (s.headdim > (1 << 20) || s.nheads > (1 << 20))
-        return fail(SSU_ERR_UNSUPPORTED, "headdim and nheads are limited to 2^20");
+    if (s.headdim > (1 << 20) || s.nheads > 65535)
+        return fail(SSU_ERR_UNSUPPORTED, "headdim is limited to 2^20 and nheads to 65535");
     if (s.batch == 0) return ok();  // nothing is read or written: strides are irrelevant
 
     const int64_t *all[] = {st->state, st->x, st->out, st->dt, st->B, st->C,

@@ -61,70 +61,68 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     const SsuParams &p = q.p;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const unsigned tile = blockIdx.x;
-    const int slab = static_cast<int>(tile % static_cast<unsigned>(p.slabs));
-    const unsigned unit = tile / static_cast<unsigned>(p.slabs);
-    const int h = static_cast<int>(unit % static_cast<unsigned>(p.nheads));
-    const long long b = static_cast<long long>(unit / static_cast<unsigned>(p.nheads));
-
-    const long long s = load_slot<kIdx64>(p, b);
-    if (s < 0 || s >= p.pool_size) {
-        if (h == 0 && slab == 0 && threadIdx.x == 0) record_skip(p, b);
-        return;
-    }
-    const int row0 = slab * p.rows_per_cta + warp * RPW;
-    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row +
-               lane_offset<NC>(lane);
-
-    float v[RPW][NC];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        if (row0 + r < p.headdim) {
-            load_cols<NC, ST>(srow + r * p.st_row, v[r]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
+    const int slab = blockIdx.x;
+    const int h = blockIdx.y;
+    for (long long b = blockIdx.z; b < p.batch; b += gridDim.z) {
+        const long long s = load_slot<kIdx64>(p, b);
+        if (s < 0 || s >= p.pool_size) {
+            if (h == 0 && slab == 0 && threadIdx.x == 0) record_skip(p, b);
+            continue;
         }
-    }
+        const int row0 = slab * p.rows_per_cta + warp * RPW;
+        ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head +
+                   row0 * p.st_row + lane_offset<NC>(lane);
 
-    const float bias = p.dt_bias[h * p.bias_h];
-    const float Ah = p.A[h * p.A_h];
-    const float Dh = p.D[h * p.D_h];
-    const int g = h / p.heads_per_group;
-    TokenIn<NC> cur = load_token<RPW, NC>(q, b, h, g, row0, 0, lane);
-    for (int t = 0; t < q.tokens; ++t) {
-        TokenIn<NC> nxt = cur;
-        if (t + 1 < q.tokens) nxt = load_token<RPW, NC>(q, b, h, g, row0, t + 1, lane);
-        const float dtv = softplus_f32(cur.dt + bias);
-        const float dA = expf(dtv * Ah);
-        float part[RPW];
+        float v[RPW][NC];
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
-            const float xr = __shfl_sync(0xffffffffu, cur.x, r);
-            part[r] = update_lane<NC>(v[r], dA, dtv * xr, cur.bb, cur.cc);
-        }
-        if (q.inter) {
-            ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
-                       row0 * q.in_p + lane_offset<NC>(lane);
+            if (row0 + r < p.headdim) {
+                load_cols<NC, ST>(srow + r * p.st_row, v[r]);
+            } else {
 #pragma unroll
-            for (int r = 0; r < RPW; ++r)
-                if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, v[r]);
+                for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
+            }
         }
-        const float total = reduce_rows<RPW>(part, lane);
-        const int rl = row_of_lane<RPW>(lane);
-        const float xr = __shfl_sync(0xffffffffu, cur.x, rl);
-        if (writes_row<RPW>(lane) && row0 + rl < p.headdim)
-            p.out[b * p.out_b + t * q.out_t + h * p.out_h + row0 + rl] =
-                __float2bfloat16_rn(fmaf(Dh, xr, total));
-        cur = nxt;
+
+        const float bias = p.dt_bias[h * p.bias_h];
+        const float Ah = p.A[h * p.A_h];
+        const float Dh = p.D[h * p.D_h];
+        const int g = h / p.heads_per_group;
+        TokenIn<NC> cur = load_token<RPW, NC>(q, b, h, g, row0, 0, lane);
+        for (int t = 0; t < q.tokens; ++t) {
+            TokenIn<NC> nxt = cur;
+            if (t + 1 < q.tokens) nxt = load_token<RPW, NC>(q, b, h, g, row0, t + 1, lane);
+            const float dtv = softplus_f32(cur.dt + bias);
+            const float dA = expf(dtv * Ah);
+            float part[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const float xr = __shfl_sync(0xffffffffu, cur.x, r);
+                part[r] = update_lane<NC>(v[r], dA, dtv * xr, cur.bb, cur.cc);
+            }
+            if (q.inter) {
+                ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
+                           row0 * q.in_p + lane_offset<NC>(lane);
+#pragma unroll
+                for (int r = 0; r < RPW; ++r)
+                    if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, v[r]);
+            }
+            const float total = reduce_rows<RPW>(part, lane);
+            const int rl = row_of_lane<RPW>(lane);
+            const float xr = __shfl_sync(0xffffffffu, cur.x, rl);
+            if (writes_row<RPW>(lane) && row0 + rl < p.headdim)
+                p.out[b * p.out_b + t * q.out_t + h * p.out_h + row0 + rl] =
+                    __float2bfloat16_rn(fmaf(Dh, xr, total));
+            cur = nxt;
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+            if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
     }
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-        if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
 }
 
 template <int NC, typename ST, bool kIdx64>
-cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, unsigned grid,
+cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, dim3 grid,
                             cudaStream_t st) {
     const dim3 block(32 * wpc);
     switch (rpw) {
@@ -138,7 +136,7 @@ cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, unsigned gri
 }
 
 cudaError_t launch_tokens(const TokenParams &q, int nc, bool bf16, bool i64, int rpw, int wpc,
-                          unsigned grid, cudaStream_t st) {
+                          dim3 grid, cudaStream_t st) {
 #define SSU_TOK_NC(NC_)                                                                      \
     if (nc == NC_) {                                                                         \
         if (bf16)                                                                            \
@@ -228,6 +226,7 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     p.A_h = strides->A[0];
     p.idx_s = strides->idx;
     p.pool_size = s.pool_size;
+    p.batch = s.batch;
     p.nheads = static_cast<int>(s.nheads);
     p.headdim = static_cast<int>(s.headdim);
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
@@ -250,10 +249,11 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     if (guard.err != cudaSuccess)
         return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
+                    static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
     const cudaError_t e = launch_tokens(q, static_cast<int>(s.dstate / 32),
                                         s.state_dtype == SSU_STATE_BF16,
-                                        s.index_dtype == SSU_INDEX_I64, rpw, wpc,
-                                        static_cast<unsigned>(tiles), cs);
+                                        s.index_dtype == SSU_INDEX_I64, rpw, wpc, grid, cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }

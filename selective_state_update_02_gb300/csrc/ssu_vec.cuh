@@ -1,4 +1,4 @@
-// VEC kernel of the decode step: one CTA per (request, head, slab of rows).  Each warp holds
+// VEC kernel of the decode step: one CTA per (slab of rows, head, request).  Each warp holds
 // RPW rows of the state in registers (all loads issued before any use), updates them, stores
 // them back in place with streaming stores and writes the readout.  Templated on the rows per
 // warp, the columns per lane (dstate = 32 * NC), the state element type (fp32 or bf16, computed
@@ -9,68 +9,70 @@
 
 namespace {
 
+// Grid: x = slab of rows, y = head, z = request (requests beyond gridDim.z loop), so the
+// slot lookup at the head of the dependency chain needs no index arithmetic.
 template <int RPW, int NC, typename ST, bool kIdx64>
 __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     ssu_vec_kernel(const __grid_constant__ SsuParams p) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const unsigned tile = blockIdx.x;
-    const int slab = static_cast<int>(tile % static_cast<unsigned>(p.slabs));
-    const unsigned unit = tile / static_cast<unsigned>(p.slabs);
-    const int h = static_cast<int>(unit % static_cast<unsigned>(p.nheads));
-    const long long b = static_cast<long long>(unit / static_cast<unsigned>(p.nheads));
-
-    const long long s = load_slot<kIdx64>(p, b);
-    if (s < 0 || s >= p.pool_size) {
-        if (h == 0 && slab == 0 && threadIdx.x == 0) record_skip(p, b);
-        return;
-    }
-
-    const int row0 = slab * p.rows_per_cta + warp * RPW;
-    ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head + row0 * p.st_row +
-               lane_offset<NC>(lane);
-
-    // Issue every state load of this warp before anything that depends on other loads.
-    float v[RPW][NC];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        if (row0 + r < p.headdim) {
-            load_cols<NC, ST>(srow + r * p.st_row, v[r]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
+    const int slab = blockIdx.x;
+    const int h = blockIdx.y;
+    for (long long b = blockIdx.z; b < p.batch; b += gridDim.z) {
+        const long long s = load_slot<kIdx64>(p, b);
+        if (s < 0 || s >= p.pool_size) {
+            if (h == 0 && slab == 0 && threadIdx.x == 0) record_skip(p, b);
+            continue;
         }
-    }
 
-    // Per-unit scalars, computed while the state loads are in flight.
-    const float z = __bfloat162float(p.dt[b * p.dt_b + h * p.dt_h]) + p.dt_bias[h * p.bias_h];
-    const float dtv = softplus_f32(z);
-    const float dA = expf(dtv * p.A[h * p.A_h]);
-    const float Dh = p.D[h * p.D_h];
-    const int g = h / p.heads_per_group;
-    float bb[NC], cc[NC];
-    load_bc<NC>(p.B + b * p.B_b + g * p.B_g + lane_offset<NC>(lane), bb);
-    load_bc<NC>(p.C + b * p.C_b + g * p.C_g + lane_offset<NC>(lane), cc);
-    const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
+        const int row0 = slab * p.rows_per_cta + warp * RPW;
+        ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head +
+                   row0 * p.st_row + lane_offset<NC>(lane);
 
-    float part[RPW];
+        // Issue every state load of this warp before anything that depends on other loads.
+        float v[RPW][NC];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        const bool live = row0 + r < p.headdim;
-        const float xr = live ? __bfloat162float(xp[r]) : 0.f;
-        part[r] = update_lane<NC>(v[r], dA, dtv * xr, bb, cc);
-        if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
-    }
-    const float total = reduce_rows<RPW>(part, lane);
-    const int rl = row_of_lane<RPW>(lane);
-    if (writes_row<RPW>(lane) && row0 + rl < p.headdim) {
-        const float xr = __bfloat162float(xp[rl]);
-        p.out[b * p.out_b + h * p.out_h + row0 + rl] = __float2bfloat16_rn(fmaf(Dh, xr, total));
+        for (int r = 0; r < RPW; ++r) {
+            if (row0 + r < p.headdim) {
+                load_cols<NC, ST>(srow + r * p.st_row, v[r]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
+            }
+        }
+
+        // Per-unit scalars, computed while the state loads are in flight.
+        const float z =
+            __bfloat162float(p.dt[b * p.dt_b + h * p.dt_h]) + p.dt_bias[h * p.bias_h];
+        const float dtv = softplus_f32(z);
+        const float dA = expf(dtv * p.A[h * p.A_h]);
+        const float Dh = p.D[h * p.D_h];
+        const int g = h / p.heads_per_group;
+        float bb[NC], cc[NC];
+        load_bc<NC>(p.B + b * p.B_b + g * p.B_g + lane_offset<NC>(lane), bb);
+        load_bc<NC>(p.C + b * p.C_b + g * p.C_g + lane_offset<NC>(lane), cc);
+        const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
+
+        float part[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const bool live = row0 + r < p.headdim;
+            const float xr = live ? __bfloat162float(xp[r]) : 0.f;
+            part[r] = update_lane<NC>(v[r], dA, dtv * xr, bb, cc);
+            if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
+        }
+        const float total = reduce_rows<RPW>(part, lane);
+        const int rl = row_of_lane<RPW>(lane);
+        if (writes_row<RPW>(lane) && row0 + rl < p.headdim) {
+            const float xr = __bfloat162float(xp[rl]);
+            p.out[b * p.out_b + h * p.out_h + row0 + rl] =
+                __float2bfloat16_rn(fmaf(Dh, xr, total));
+        }
     }
 }
 
 template <int NC, typename ST, bool kIdx64>
-cudaError_t launch_vec_t(const SsuParams &p, int rpw, int wpc, unsigned grid, cudaStream_t st) {
+cudaError_t launch_vec_t(const SsuParams &p, int rpw, int wpc, dim3 grid, cudaStream_t st) {
     const dim3 block(32 * wpc);
     switch (rpw) {
         case 1: ssu_vec_kernel<1, NC, ST, kIdx64><<<grid, block, 0, st>>>(p); break;
@@ -91,7 +93,7 @@ cudaError_t launch_vec_t(const SsuParams &p, int rpw, int wpc, unsigned grid, cu
 
 // Launches the VEC kernel for dstate = 32 * nc, a bf16 or fp32 state, int64 or int32 indices.
 inline cudaError_t launch_vec(const SsuParams &p, int nc, bool bf16, bool i64, int rpw, int wpc,
-                              unsigned grid, cudaStream_t st) {
+                              dim3 grid, cudaStream_t st) {
 #define SSU_VEC_NC(NC_)                                                                     \
     if (nc == NC_) {                                                                        \
         if (bf16)                                                                           \

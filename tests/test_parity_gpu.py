@@ -356,3 +356,13 @@ def test_head_sweep_batch_256(op, H):
     mask[idx] = False
     keep = torch.from_numpy(np.nonzero(mask)[0]).to(DEV)
     assert torch.equal(pool_d[keep], torch.from_numpy(pool[mask]).to(DEV))
+
+
+def test_batch_beyond_one_grid_dimension(op):
+    # 70,000 requests: more than one grid dimension holds, so the kernel loops over requests.
+    bs = 70000
+    pr = wl.make_problem(bs, 1, P=2, pool_size=bs + 10, seed=41)
+    t = to_device(pr, DEV)
+    _run(op, t)
+    assert op.get_error() == (0, -1)
+    _compare_all(pr, t, pr.pool)
