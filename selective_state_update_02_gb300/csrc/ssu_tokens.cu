@@ -33,6 +33,27 @@ struct TokenParams {
     int tokens;
 };
 
+// update_lane (ssu_device.cuh) with the state update in packed fp32x2 instructions (two IEEE round-to-nearest
+// multiplies and two fused multiply-adds per pair of columns): the same values bit for bit,
+// with half the instructions for the update.  The readout chain stays scalar, in the same
+// order.  Used where instruction issue, not memory, bounds the kernel (the multi-token loop).
+template <int NC>
+__device__ __forceinline__ float update_lane_packed(float (&v)[NC], float dA, float k,
+                                                    const float (&bb)[NC], const float (&cc)[NC]) {
+    const float2 dA2 = make_float2(dA, dA), k2 = make_float2(k, k);
+#pragma unroll
+    for (int j = 0; j < NC; j += 2) {
+        const float2 kb = __fmul2_rn(k2, make_float2(bb[j], bb[j + 1]));
+        const float2 r = __ffma2_rn(make_float2(v[j], v[j + 1]), dA2, kb);
+        v[j] = r.x;
+        v[j + 1] = r.y;
+    }
+    float part = v[0] * cc[0];
+#pragma unroll
+    for (int j = 1; j < NC; ++j) part = fmaf(v[j], cc[j], part);
+    return part;
+}
+
 // One token's inputs for one warp: lane r < RPW holds x of row r.
 template <int NC>
 struct TokenIn {
@@ -98,7 +119,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
                 const float xr = __shfl_sync(0xffffffffu, cur.x, r);
-                part[r] = update_lane<NC>(v[r], dA, dtv * xr, cur.bb, cur.cc);
+                part[r] = update_lane_packed<NC>(v[r], dA, dtv * xr, cur.bb, cur.cc);
             }
             if (q.inter) {
                 ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
