@@ -71,16 +71,19 @@ bool launch_shape_ok(const ssu_launch_t &l) {
 
 namespace {
 
-// Built-in launch-shape table, from the cold-L2 sweep on GB300 (bench.py --sweep): the VEC
-// kernel with 8 rows per warp (8 x 16-byte loads in flight per thread) is fastest at batch 8,
-// 128 and 512, and 1 to 4 warps per CTA are within 0.2% of each other; 2 warps is used.  For
-// a headdim below 16 the tile shrinks to the largest power of two that fits.
+// Built-in launch-shape table, from the cold-L2 sweeps on GB300 (bench.py --sweep, with and
+// without --dstate / --state-dtype).  The VEC kernel with 8 rows per warp and 2 warps per CTA
+// is fastest from batch 32 up (dstate 256: 4 rows per warp, fewer registers).  A call too
+// small to give every SM 16 warps at that size steps down to 4, then 2 rows per warp with 4
+// warps per CTA (batch 8: 3.80 us instead of 3.97).  The tile never exceeds the headdim.
 ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
-    (void)hd;
     (void)st;
-    int rpw = 8;
+    int rpw = s.dstate == 256 ? 4 : 8;
+    const long long rows = s.batch * s.nheads * s.headdim;
+    while (rpw > 2 && rows / rpw < 16LL * hd.sm_count) rpw >>= 1;
     while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
-    const int wpc = s.headdim >= 2 * rpw ? 2 : 1;
+    int wpc = rpw <= 2 ? 4 : 2;
+    while (wpc > 1 && rpw * wpc > s.headdim) wpc >>= 1;
     return ssu_launch_t{SSU_MODE_VEC, rpw, wpc, 0};
 }
 

@@ -366,3 +366,36 @@ def test_batch_beyond_one_grid_dimension(op):
     _run(op, t)
     assert op.get_error() == (0, -1)
     _compare_all(pr, t, pr.pool)
+
+
+def test_pool_beyond_2_31_elements(op):
+    # 16400 slots x 16 heads x 64 x 128 fp32 (512 KiB per slot) = 8.6 GB: slots from 16384 on
+    # start beyond 2^31 elements, so the address arithmetic must be 64-bit.  Only the touched
+    # slots hold seeded values (written from the host); the rest is zero and must stay zero.
+    slots, H, bs = 16400, 16, 6
+    if torch.cuda.get_device_properties(0).total_memory < 32 * 2 ** 30:
+        pytest.skip("needs a large device")
+    rng = np.random.default_rng(77)
+    per_slot = H * 64 * 128
+    assert 16384 * per_slot == 2 ** 31
+    idx = np.array([16399, 16384, 16383, 16390, 17, 9000], dtype=np.int64)
+    sub = wl.state_pool(rng, bs, H)                              # the touched slots' states
+    dt_bias, A, D = wl.head_params(rng, H)
+    x, dt, B, C = wl.request_inputs(rng, bs, H)
+    pool = torch.zeros(slots, H, 64, 128, device=DEV)
+    pool[torch.from_numpy(idx).to(DEV)] = torch.from_numpy(sub).to(DEV)
+    out = torch.zeros(bs, H, 64, dtype=torch.bfloat16, device=DEV)
+    op(pool, torch.from_numpy(idx).to(DEV), bf16_tensor(x, DEV), bf16_tensor(dt, DEV),
+       torch.from_numpy(dt_bias).to(DEV), torch.from_numpy(A).to(DEV), bf16_tensor(B, DEV),
+       bf16_tensor(C, DEV), torch.from_numpy(D).to(DEV), out)
+    torch.cuda.synchronize()
+    ref_states, ref_y = oracle_on_requests(sub, np.arange(bs), np.arange(bs), x, dt, dt_bias, A,
+                                           B, C, D)
+    check_state(pool[torch.from_numpy(idx).to(DEV)].cpu().numpy(), ref_states)
+    Ch, Dx = expected_terms(x, D, C, 1, H)
+    check_y(bits_of(out), ref_y, ref_states, Ch, Dx, 128)
+    mask = torch.ones(slots, dtype=torch.bool, device=DEV)
+    mask[torch.from_numpy(idx).to(DEV)] = False
+    assert not pool[mask].any()
+    del pool
+    torch.cuda.empty_cache()
