@@ -180,6 +180,16 @@ ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch);
 ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
                             ssu_launch_t *launch);
 
+/*
+ * Opt in (enable != 0) or out of programmatic dependent launch for this handle's VEC and
+ * multi-token launches (default: out).  A launch may then be scheduled while the previous
+ * kernel in the stream is finishing; the kernel's first instruction waits for that kernel to
+ * complete and its memory to be visible, so results are unchanged, and each CTA releases its
+ * own dependents once its stores are issued.  This hides part of the launch gap between
+ * back-to-back kernels.  BULK, copy and allocation-free launches never use it.
+ */
+ssu_status_t ssu_set_pdl(ssu_handle_t handle, int32_t enable);
+
 /* ---------------------------------------------------------------------------------------
  * Multi-token step: T consecutive tokens of every request in one call, as multi-token
  * speculation verifies them (vLLM PR #48110, Test Plan: speculative decoding with two draft

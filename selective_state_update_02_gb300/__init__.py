@@ -108,6 +108,7 @@ _EXPORTS = {
     "ssu_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_launch_t)]),
     "ssu_get_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_shape_t),
                                       ctypes.POINTER(ssu_launch_t)]),
+    "ssu_set_pdl": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "ssu_update_tokens": (ctypes.c_int, [_vp] * 12 + [ctypes.POINTER(ssu_shape_t),
                                                       ctypes.POINTER(ssu_strides_t),
                                                       ctypes.c_int64,
@@ -316,6 +317,11 @@ def ssu_set_launch(handle: int, mode: int = SSU_MODE_AUTO, rows_per_warp: int = 
     """Force a launch shape (mode AUTO restores the built-in table)."""
     cfg = ssu_launch_t(mode, rows_per_warp, warps_per_cta, stages)
     _check(lib().ssu_set_launch(handle, ctypes.byref(cfg)), "ssu_set_launch")
+
+
+def ssu_set_pdl(handle: int, enable: bool = True) -> None:
+    """Opt in or out of programmatic dependent launch for this handle (off by default)."""
+    _check(lib().ssu_set_pdl(handle, 1 if enable else 0), "ssu_set_pdl")
 
 
 def ssu_get_launch(handle: int, shape: ssu_shape_t) -> tuple[int, int, int, int]:

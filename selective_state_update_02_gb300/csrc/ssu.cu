@@ -182,6 +182,12 @@ ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch) {
     return ok();
 }
 
+ssu_status_t ssu_set_pdl(ssu_handle_t handle, int32_t enable) {
+    if (!handle) return fail(SSU_ERR_INVALID_ARG, "NULL handle");
+    handle->pdl = enable != 0;
+    return ok();
+}
+
 ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state_batch_indices,
                         const uint16_t *x, const uint16_t *dt, const float *dt_bias,
                         const float *A, const uint16_t *B, const uint16_t *C, const float *D,
@@ -270,7 +276,7 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
         const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
                         static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
         e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16, i64,
-                       l.rows_per_warp, l.warps_per_cta, grid, cs);
+                       l.rows_per_warp, l.warps_per_cta, grid, handle->pdl, cs);
     }
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
@@ -418,7 +424,7 @@ extern "C" ssu_status_t ssu_update_static(void *state_pool, const void *state_ba
                        s.index_dtype == SSU_INDEX_I64, l.rows_per_warp, l.warps_per_cta,
                        dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
                             static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535)),
-                       cs);
+                       false, cs);
     if (e == cudaSuccess && counters_out)
         e = cudaMemcpyAsync(counters_out, scratch, 3 * sizeof(unsigned),
                             cudaMemcpyDeviceToDevice, cs);

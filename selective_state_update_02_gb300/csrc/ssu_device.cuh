@@ -206,6 +206,18 @@ __device__ __forceinline__ bool writes_row(int lane) {
     return (lane & (32 / R - 1)) == 0;
 }
 
+// Programmatic dependent launch.  pdl_wait blocks until the grid this one depends on has
+// completed and its memory is visible (a no-op when the launch carries no such dependency);
+// kernels call it before their first memory access, so a dependent launch never reads or
+// writes anything early.  pdl_trigger lets the dependent grid's CTAs start launching.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <bool kIdx64>
 __device__ __forceinline__ long long load_slot(const SsuParams &p, long long b) {
     if (kIdx64) return __ldg(static_cast<const long long *>(p.idx) + b * p.idx_s);

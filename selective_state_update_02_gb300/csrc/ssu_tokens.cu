@@ -79,6 +79,7 @@ __device__ __forceinline__ TokenIn<NC> load_token(const TokenParams &q, long lon
 template <int RPW, int NC, typename ST, bool kIdx64>
 __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     ssu_tokens_kernel(const __grid_constant__ TokenParams q) {
+    pdl_wait();
     const SsuParams &p = q.p;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -140,31 +141,47 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         for (int r = 0; r < RPW; ++r)
             if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
     }
+    pdl_trigger();  // this CTA's stores are issued: a dependent launch may start its CTAs
+}
+
+template <int RPW, int NC, typename ST, bool kIdx64>
+cudaError_t launch_tokens_one(const TokenParams &q, dim3 grid, dim3 block, bool pdl,
+                              cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, ssu_tokens_kernel<RPW, NC, ST, kIdx64>, q);
 }
 
 template <int NC, typename ST, bool kIdx64>
-cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, dim3 grid,
+cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, dim3 grid, bool pdl,
                             cudaStream_t st) {
     const dim3 block(32 * wpc);
     switch (rpw) {
-        case 1: ssu_tokens_kernel<1, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
-        case 2: ssu_tokens_kernel<2, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
-        case 4: ssu_tokens_kernel<4, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
-        case 8: ssu_tokens_kernel<8, NC, ST, kIdx64><<<grid, block, 0, st>>>(q); break;
+        case 1: return launch_tokens_one<1, NC, ST, kIdx64>(q, grid, block, pdl, st);
+        case 2: return launch_tokens_one<2, NC, ST, kIdx64>(q, grid, block, pdl, st);
+        case 4: return launch_tokens_one<4, NC, ST, kIdx64>(q, grid, block, pdl, st);
+        case 8: return launch_tokens_one<8, NC, ST, kIdx64>(q, grid, block, pdl, st);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_tokens(const TokenParams &q, int nc, bool bf16, bool i64, int rpw, int wpc,
-                          dim3 grid, cudaStream_t st) {
+                          dim3 grid, bool pdl, cudaStream_t st) {
 #define SSU_TOK_NC(NC_)                                                                      \
     if (nc == NC_) {                                                                         \
         if (bf16)                                                                            \
-            return i64 ? launch_tokens_t<NC_, __nv_bfloat16, true>(q, rpw, wpc, grid, st)    \
-                       : launch_tokens_t<NC_, __nv_bfloat16, false>(q, rpw, wpc, grid, st);  \
-        return i64 ? launch_tokens_t<NC_, float, true>(q, rpw, wpc, grid, st)                \
-                   : launch_tokens_t<NC_, float, false>(q, rpw, wpc, grid, st);              \
+            return i64 ? launch_tokens_t<NC_, __nv_bfloat16, true>(q, rpw, wpc, grid, pdl, st) \
+                       : launch_tokens_t<NC_, __nv_bfloat16, false>(q, rpw, wpc, grid, pdl,    \
+                                                                    st);                       \
+        return i64 ? launch_tokens_t<NC_, float, true>(q, rpw, wpc, grid, pdl, st)             \
+                   : launch_tokens_t<NC_, float, false>(q, rpw, wpc, grid, pdl, st);           \
     }
     SSU_TOK_NC(2)
     SSU_TOK_NC(4)
@@ -274,7 +291,8 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                     static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
     const cudaError_t e = launch_tokens(q, static_cast<int>(s.dstate / 32),
                                         s.state_dtype == SSU_STATE_BF16,
-                                        s.index_dtype == SSU_INDEX_I64, rpw, wpc, grid, cs);
+                                        s.index_dtype == SSU_INDEX_I64, rpw, wpc, grid,
+                                        handle->pdl, cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -14,6 +14,7 @@ namespace {
 template <int RPW, int NC, typename ST, bool kIdx64>
 __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
     ssu_vec_kernel(const __grid_constant__ SsuParams p) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int slab = blockIdx.x;
@@ -69,38 +70,53 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
                 __float2bfloat16_rn(fmaf(Dh, xr, total));
         }
     }
+    pdl_trigger();  // this CTA's stores are issued: a dependent launch may start its CTAs
+}
+
+// Launches one instantiation; with `pdl` the launch may begin before the previous kernel in
+// the stream has finished (the kernel waits for it before touching memory).
+template <int RPW, int NC, typename ST, bool kIdx64>
+cudaError_t launch_vec_one(const SsuParams &p, dim3 grid, dim3 block, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, ssu_vec_kernel<RPW, NC, ST, kIdx64>, p);
 }
 
 template <int NC, typename ST, bool kIdx64>
-cudaError_t launch_vec_t(const SsuParams &p, int rpw, int wpc, dim3 grid, cudaStream_t st) {
+cudaError_t launch_vec_t(const SsuParams &p, int rpw, int wpc, dim3 grid, bool pdl,
+                         cudaStream_t st) {
     const dim3 block(32 * wpc);
     switch (rpw) {
-        case 1: ssu_vec_kernel<1, NC, ST, kIdx64><<<grid, block, 0, st>>>(p); break;
-        case 2: ssu_vec_kernel<2, NC, ST, kIdx64><<<grid, block, 0, st>>>(p); break;
-        case 4: ssu_vec_kernel<4, NC, ST, kIdx64><<<grid, block, 0, st>>>(p); break;
-        case 8: ssu_vec_kernel<8, NC, ST, kIdx64><<<grid, block, 0, st>>>(p); break;
+        case 1: return launch_vec_one<1, NC, ST, kIdx64>(p, grid, block, pdl, st);
+        case 2: return launch_vec_one<2, NC, ST, kIdx64>(p, grid, block, pdl, st);
+        case 4: return launch_vec_one<4, NC, ST, kIdx64>(p, grid, block, pdl, st);
+        case 8: return launch_vec_one<8, NC, ST, kIdx64>(p, grid, block, pdl, st);
         case 16:
-            if constexpr (NC == 4 && sizeof(ST) == 4) {
-                ssu_vec_kernel<16, NC, ST, kIdx64><<<grid, block, 0, st>>>(p);
-                break;
-            } else {
+            if constexpr (NC == 4 && sizeof(ST) == 4)
+                return launch_vec_one<16, NC, ST, kIdx64>(p, grid, block, pdl, st);
+            else
                 return cudaErrorInvalidValue;
-            }
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 // Launches the VEC kernel for dstate = 32 * nc, a bf16 or fp32 state, int64 or int32 indices.
 inline cudaError_t launch_vec(const SsuParams &p, int nc, bool bf16, bool i64, int rpw, int wpc,
-                              dim3 grid, cudaStream_t st) {
+                              dim3 grid, bool pdl, cudaStream_t st) {
 #define SSU_VEC_NC(NC_)                                                                     \
     if (nc == NC_) {                                                                        \
         if (bf16)                                                                           \
-            return i64 ? launch_vec_t<NC_, __nv_bfloat16, true>(p, rpw, wpc, grid, st)      \
-                       : launch_vec_t<NC_, __nv_bfloat16, false>(p, rpw, wpc, grid, st);    \
-        return i64 ? launch_vec_t<NC_, float, true>(p, rpw, wpc, grid, st)                  \
-                   : launch_vec_t<NC_, float, false>(p, rpw, wpc, grid, st);                \
+            return i64 ? launch_vec_t<NC_, __nv_bfloat16, true>(p, rpw, wpc, grid, pdl, st) \
+                       : launch_vec_t<NC_, __nv_bfloat16, false>(p, rpw, wpc, grid, pdl, st); \
+        return i64 ? launch_vec_t<NC_, float, true>(p, rpw, wpc, grid, pdl, st)             \
+                   : launch_vec_t<NC_, float, false>(p, rpw, wpc, grid, pdl, st);           \
     }
     SSU_VEC_NC(2)
     SSU_VEC_NC(4)

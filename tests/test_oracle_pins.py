@@ -351,3 +351,37 @@ def test_copy_blocks_skips_requests_out_of_any_range():
     assert skipped == 2
     np.testing.assert_array_equal(na[0], [5, 5])
     np.testing.assert_array_equal(na[2], [0, 0])
+
+
+def test_tokens_oracle_matches_the_unrolled_recurrence_at_every_token():
+    # oracle.ssu_tokens: intermediate state after token t equals
+    #   (prod_{u<=t} dA_u) S_0 + sum_{v<=t} (prod_{v<u<=t} dA_u) dt_v x_v (x) B_v,
+    # and y_t = S_t C_t + D x_t; requests with an out-of-range slot are skipped.
+    T, bs, H, P, N = 4, 3, 2, 3, 8
+    rng = np.random.default_rng(31)
+    pool = rng.standard_normal((5, H, P, N))
+    idx = np.array([3, 0, 9])                       # request 2 names no slot
+    dt_bias, A, D = wl.head_params(rng, H)
+    steps = [wl.request_inputs(rng, bs, H, P, N, 1) for _ in range(T)]
+    x, dt, B, C = (np.stack([s[k] for s in steps], 1) for k in range(4))
+    new_pool, y, inter, skipped = oracle.ssu_tokens(pool, idx, x, dt, dt_bias, A, B, C, D)
+    assert skipped == 1 and np.isnan(inter[2]).all()
+    for b in (0, 1):
+        S = pool[idx[b]].copy()
+        dA_list, terms = [], []
+        for t in range(T):
+            z = oracle.bf16_to_f64(dt[b, t]) + dt_bias.astype(np.float64)
+            dtv = _softplus_lib(z)
+            dA_list.append(np.exp(dtv * A.astype(np.float64)))
+            xf = oracle.bf16_to_f64(x[b, t])
+            Bf = oracle.bf16_to_f64(B[b, t, 0])
+            terms.append(dtv[:, None, None] * xf[:, :, None] * Bf[None, None, :])
+            closed = np.prod(dA_list, axis=0)[:, None, None] * S
+            for v in range(t + 1):
+                decay = np.prod(dA_list[v + 1:t + 1], axis=0) if v < t else np.ones(H)
+                closed = closed + decay[:, None, None] * terms[v]
+            np.testing.assert_allclose(inter[b, t], closed, rtol=1e-12, atol=1e-12)
+            yt = closed @ oracle.bf16_to_f64(C[b, t, 0]) + D.astype(np.float64)[:, None] * xf
+            np.testing.assert_allclose(y[b, t], yt, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(new_pool[idx[b]], inter[b, T - 1], rtol=0, atol=0)
+    np.testing.assert_array_equal(new_pool[[1, 2, 4]], pool[[1, 2, 4]])
