@@ -437,9 +437,17 @@ def cpu_baseline(bs: int, H: int, budget_s: float = 12.0) -> dict:
     while time.perf_counter() - t_start < budget_s and len(times) < 50:
         times.append(oc.run())
     med = statistics.median(times)
+    # the same oracle on one thread, over a quarter of the batch (scaled to the full call)
+    threads, oc.threads = oc.threads, 1
+    quarter = max(1, bs // 4)
+    single = [oc.run(quarter) * (bs / quarter) for _ in range(3)]
+    oc.threads = threads
     return {"value": round(med * 1e6, 1), "unit": UNIT, "cores": oc.threads, "kind": "oracle",
             "sample": f"{len(times)} full calls (batch {bs}, {H} heads, headdim 64, dstate 128) "
-                      f"of the fp64 C oracle split over {oc.threads} host threads; median"}
+                      f"of the fp64 C oracle split over {oc.threads} host threads; median",
+            "single_thread_value": round(statistics.median(single) * 1e6, 1),
+            "single_thread_sample": f"3 calls over {quarter} of the {bs} requests on one "
+                                    f"thread, scaled to the full batch; median"}
 
 
 # ---- main ---------------------------------------------------------------------------------
@@ -805,7 +813,12 @@ def run_tokens(args) -> None:
     w = Workload(bs, H, dev, seed=5, l2_bytes=l2)
     rng = np.random.default_rng(9)
     peaks = load_peaks()
-    for T in (1, 2, 3, 4):
+    shapes = [None]
+    tokens_list = (1, 2, 3, 4)
+    if args.sweep:
+        shapes = [(r, w) for r in (4, 8, 16) for w in (1, 2, 4)]
+        tokens_list = (2, 4)
+    for T in tokens_list:
         x = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(
             (w.n_sets, bs, T, H, HEADDIM), dtype=np.float32)).view(np.int16)).view(
             torch.bfloat16).to(dev)
@@ -816,7 +829,12 @@ def run_tokens(args) -> None:
             -4, 0, (w.n_sets, bs, T, H)).astype(np.float32)).view(np.int16)).view(
             torch.bfloat16).to(dev)
         out = torch.empty(bs, T, H, HEADDIM, dtype=torch.bfloat16, device=dev)
-        for with_inter in (False, True):
+        for shape, with_inter in [(sh, wi) for sh in shapes
+                                  for wi in ((False,) if args.sweep else (False, True))]:
+            if shape is None:
+                ssu.ssu_set_launch(handle, ssu.SSU_MODE_AUTO)
+            else:
+                ssu.ssu_set_launch(handle, ssu.SSU_MODE_VEC, shape[0], shape[1])
             inter = (torch.empty(bs, T, H, HEADDIM, DSTATE, device=dev) if with_inter else None)
 
             def call(i, stream_ptr, T=T, x=x, bc=bc, dt=dt, out=out, inter=inter):
@@ -830,6 +848,7 @@ def run_tokens(args) -> None:
             moved = bytes_per_call_tokens(bs, T, with_inter)
             gbs = moved / (us * 1e-6) / 1e9
             print(json.dumps({"tokens": T, "batch": bs, "intermediate": with_inter,
+                              "launch": list(shape) if shape else "table",
                               "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
                               "gbs": round(gbs, 1),
                               "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4)}),

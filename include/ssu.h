@@ -170,6 +170,16 @@ ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *s
                            int64_t *first_bad);
 
 /*
+ * Debug check of a HOST copy of state_batch_indices (it is never read from the device):
+ * every id must lie in [0, pool_size) and no id may repeat (two requests naming one slot
+ * would update it concurrently, a data race ssu_update does not detect).  Returns SSU_OK, or
+ * SSU_ERR_INVALID_ARG with *first_bad (may be NULL) set to the index i of the first entry
+ * that is out of range or repeats an earlier one.  Allocates host memory only.
+ */
+ssu_status_t ssu_check_indices(const void *host_indices, int64_t n, int32_t index_dtype,
+                               int64_t pool_size, int64_t *first_bad);
+
+/*
  * Force a launch shape for later ssu_update calls on this handle (for sweeps and tests).
  * NULL, or mode SSU_MODE_AUTO, restores the built-in table.  Every accepted shape computes
  * bit-identical results: each row's readout is summed in one fixed order.

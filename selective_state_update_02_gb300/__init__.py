@@ -109,6 +109,8 @@ _EXPORTS = {
     "ssu_get_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_shape_t),
                                       ctypes.POINTER(ssu_launch_t)]),
     "ssu_set_pdl": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "ssu_check_indices": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64,
+                                         ctypes.POINTER(ctypes.c_int64)]),
     "ssu_update_tokens": (ctypes.c_int, [_vp] * 12 + [ctypes.POINTER(ssu_shape_t),
                                                       ctypes.POINTER(ssu_strides_t),
                                                       ctypes.c_int64,
@@ -317,6 +319,24 @@ def ssu_set_launch(handle: int, mode: int = SSU_MODE_AUTO, rows_per_warp: int = 
     """Force a launch shape (mode AUTO restores the built-in table)."""
     cfg = ssu_launch_t(mode, rows_per_warp, warps_per_cta, stages)
     _check(lib().ssu_set_launch(handle, ctypes.byref(cfg)), "ssu_set_launch")
+
+
+def ssu_check_indices(state_batch_indices, pool_size: int) -> int:
+    """Debug check of a host (CPU) index tensor: in range and no repeated slot.  Returns -1
+    when the indices are valid, else the position of the first bad entry."""
+    t = state_batch_indices
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or t.dim() != 1:
+        raise TypeError("state_batch_indices must be a 1-D CPU tensor")
+    if t.dtype not in (torch.int32, torch.int64):
+        raise TypeError("state_batch_indices must be int32 or int64")
+    t = t.contiguous()
+    first = ctypes.c_int64(-1)
+    st = lib().ssu_check_indices(t.data_ptr(), t.shape[0],
+                                 SSU_INDEX_I64 if t.dtype == torch.int64 else SSU_INDEX_I32,
+                                 int(pool_size), ctypes.byref(first))
+    if st not in (SSU_OK, SSU_ERR_INVALID_ARG):
+        _check(st, "ssu_check_indices")
+    return int(first.value) if st != SSU_OK else -1
 
 
 def ssu_set_pdl(handle: int, enable: bool = True) -> None:

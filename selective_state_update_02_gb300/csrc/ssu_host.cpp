@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <string>
+#include <vector>
 
 #include "ssu_host.h"
 
@@ -117,5 +118,37 @@ const char *ssu_status_string(ssu_status_t status) {
 }
 
 const char *ssu_last_error(void) { return ssu_host::g_last_error.c_str(); }
+
+ssu_status_t ssu_check_indices(const void *host_indices, int64_t n, int32_t index_dtype,
+                               int64_t pool_size, int64_t *first_bad) {
+    using ssu_host::fail;
+    if (first_bad) *first_bad = -1;
+    if (n < 0 || pool_size < 0) return fail(SSU_ERR_INVALID_ARG, "n and pool_size must be >= 0");
+    if (index_dtype != SSU_INDEX_I32 && index_dtype != SSU_INDEX_I64)
+        return fail(SSU_ERR_INVALID_ARG, "index_dtype %d is neither I32 nor I64", index_dtype);
+    if (n == 0) return ssu_host::ok();
+    if (!host_indices) return fail(SSU_ERR_INVALID_ARG, "host_indices is NULL");
+    // One bit per slot marks the slots seen so far.
+    std::vector<unsigned char> seen(static_cast<size_t>((pool_size + 7) / 8), 0);
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t s = index_dtype == SSU_INDEX_I64
+                              ? static_cast<const int64_t *>(host_indices)[i]
+                              : static_cast<int64_t>(static_cast<const int32_t *>(host_indices)[i]);
+        if (s < 0 || s >= pool_size) {
+            if (first_bad) *first_bad = i;
+            return fail(SSU_ERR_INVALID_ARG, "request %lld names slot %lld outside [0, %lld)",
+                        (long long)i, (long long)s, (long long)pool_size);
+        }
+        unsigned char &byte = seen[static_cast<size_t>(s >> 3)];
+        const unsigned char bit = static_cast<unsigned char>(1u << (s & 7));
+        if (byte & bit) {
+            if (first_bad) *first_bad = i;
+            return fail(SSU_ERR_INVALID_ARG, "request %lld repeats slot %lld", (long long)i,
+                        (long long)s);
+        }
+        byte |= bit;
+    }
+    return ssu_host::ok();
+}
 
 }  // extern "C"

@@ -76,8 +76,15 @@ __device__ __forceinline__ TokenIn<NC> load_token(const TokenParams &q, long lon
     return in;
 }
 
+// 16 rows per warp hold 64 state values per lane: those CTAs are limited to 4 warps so the
+// compiler may use up to 255 registers without spilling.
+template <int RPW>
+constexpr int tokens_max_threads() {
+    return RPW >= 16 ? 128 : 32 * kMaxWarpsPerCta;
+}
+
 template <int RPW, int NC, typename ST, bool kIdx64>
-__global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
+__global__ void __launch_bounds__(tokens_max_threads<RPW>())
     ssu_tokens_kernel(const __grid_constant__ TokenParams q) {
     pdl_wait();
     const SsuParams &p = q.p;
@@ -168,6 +175,13 @@ cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, dim3 grid, b
         case 2: return launch_tokens_one<2, NC, ST, kIdx64>(q, grid, block, pdl, st);
         case 4: return launch_tokens_one<4, NC, ST, kIdx64>(q, grid, block, pdl, st);
         case 8: return launch_tokens_one<8, NC, ST, kIdx64>(q, grid, block, pdl, st);
+        case 16:
+            if constexpr (NC <= 4)
+                return static_cast<int>(block.x) <= tokens_max_threads<16>()
+                           ? launch_tokens_one<16, NC, ST, kIdx64>(q, grid, block, pdl, st)
+                           : cudaErrorInvalidValue;
+            else
+                return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -224,11 +238,19 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
             return fail(SSU_ERR_MISALIGNED, "intermediate is not 16-byte aligned");
     }
     const ssu_shape_t &s = *shape;
-    // 8 rows per warp and 2 warps per CTA, as the single-token table (fewer rows for a small
-    // headdim).
+    // 8 rows per warp, one warp per CTA (fewer rows for a small headdim), or the handle's VEC
+    // override for sweeps (16 rows per warp for dstate up to 128).
     int rpw = 8;
     while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
-    const int wpc = s.headdim >= 2 * rpw ? 2 : 1;
+    int wpc = 1;
+    if (handle->has_override && handle->override_launch.mode == SSU_MODE_VEC) {
+        rpw = handle->override_launch.rows_per_warp;
+        wpc = handle->override_launch.warps_per_cta;
+        if (rpw > 16 || (rpw == 16 && (s.dstate > 128 || wpc > 4)))
+            return fail(SSU_ERR_UNSUPPORTED,
+                        "the multi-token kernel takes 1..8 rows per warp (16 with at most 4 "
+                        "warps, up to dstate 128)");
+    }
     const int rows_per_tile = rpw * wpc;
     const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
     const long long tiles = s.batch * s.nheads * slabs;

@@ -198,3 +198,21 @@ def test_describe_rejects_wrong_dtypes(ssu):
                      torch.zeros(2), torch.zeros(2),
                      torch.zeros(2, 1, 128, dtype=torch.bfloat16),
                      torch.zeros(2, 1, 128, dtype=torch.bfloat16), torch.zeros(2), x)
+
+
+def test_check_indices_finds_repeats_and_out_of_range(ssu):
+    import numpy as np
+    ok = torch.from_numpy(np.random.default_rng(0).permutation(1000)[:300].astype(np.int32))
+    assert ssu.ssu_check_indices(ok, 1000) == -1
+    assert ssu.ssu_check_indices(ok.to(torch.int64), 1000) == -1
+    rep = ok.clone()
+    rep[200] = rep[17]
+    assert ssu.ssu_check_indices(rep, 1000) == 200
+    oob = ok.clone()
+    oob[5] = 1000
+    assert ssu.ssu_check_indices(oob, 1000) == 5
+    neg = ok.to(torch.int64)
+    neg[9] = -1
+    assert ssu.ssu_check_indices(neg, 1000) == 9
+    assert ssu.ssu_check_indices(torch.zeros(0, dtype=torch.int32), 0) == -1
+    assert ssu.ssu_check_indices(rep, 1000) == 200 and "repeats slot" in ssu.last_error()
