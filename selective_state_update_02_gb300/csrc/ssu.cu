@@ -1,34 +1,20 @@
-// Mamba2 decode-step selective state update for GB300 (sm_103a): kernels and the C ABI.
+// Mamba2 decode-step selective state update for GB300 (sm_103a): the single-step C ABI
+// (handles, validation, launch table, ssu_update, error counters, the allocation-free entry).
 //
 // The operation and its operands are documented in include/ssu.h (sglang PR #41223,
 // Summary and Details / Kernel measurement give the operand set; the arithmetic is the
 // standard Mamba2 decode step).  The step is bound by HBM traffic: per (request, head) unit it
 // reads and writes a 64 x 128 fp32 state (32 KiB each way) and touches ~2.5 KiB of inputs.
-// There is no dense contraction here, so no tensor cores: the design goal is to keep enough
-// bytes in flight to saturate HBM3e.
+// There is no dense contraction here, so no tensor cores.
 //
-// Element mapping shared by both kernels.  A state row is dstate = 128 fp32 = 512 bytes; lane
-// l of a warp owns columns 4l..4l+3 of a row, so one row is one fully used 512-byte access per
-// warp.  B[n] and C[n] are read straight into registers (each lane needs only its own 4
-// columns); x[p], dt, dt_bias, A and D are per-tile scalars.  Each element is updated as
-// fmaf(S, dA, (dtv * x[p]) * B[n]); each row's readout is the lane's 4-term chain followed by a
-// xor butterfly over the 32 lanes in the fixed mask order 16, 8, 4, 2, 1.  Nothing in that
-// order depends on the launch shape, so every shape of both kernels gives bit-identical state
-// and output.
-//
-// VEC kernel: one CTA per (request, head, slab of rows).  Each warp loads RPW rows as 16-byte
-// vectors into registers (all loads issued before any use), updates them, stores them back in
-// place and writes the readout.  Bytes in flight are bounded by registers and occupancy.
-//
-// BULK kernel: persistent CTAs (as many as fit on the SMs) stream tiles of `tile_rows` rows
-// through a ring of shared-memory stages.  Warp 0 is the producer: it reads the slot index of
-// each tile ahead of time and issues a bulk asynchronous copy (the TMA engine's 1-D
-// `cp.async.bulk`) of the tile's contiguous rows into a free stage, completion counted on the
-// stage's mbarrier.  The compute warps read their rows out of the stage into registers, hand
-// the stage back at once (the producer refills it while they work), update the rows and store
-// them in place with 16-byte vector stores, and write the readout.  Loads in flight are bounded
-// by shared memory (stages x tile), not by registers.  Every mbarrier wait is bounded in time;
-// a timeout raises an error counter and the CTA stops after its copies in flight have landed.
+// Two kernels compute it, with the same element mapping and arithmetic (ssu_device.cuh), so
+// every launch shape of either gives bit-identical state and output:
+//   * VEC (ssu_vec.cuh): one CTA per (slab of rows, head, request); each warp holds its rows
+//     in registers, 16-byte vector loads all issued before any use.  The built-in table uses it.
+//   * BULK (ssu_bulk.cuh, fp32 and dstate 128 only): persistent CTAs stream tiles through a
+//     ring of shared-memory stages fed by the TMA engine's 1-D bulk copies; measured slower
+//     than VEC at every size and kept as a forced launch shape.
+// The multi-token step and the state-block copy live in ssu_tokens.cu and ssu_copy.cu.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

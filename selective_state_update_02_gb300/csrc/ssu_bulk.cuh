@@ -1,6 +1,13 @@
-// BULK kernel of the decode step (fp32 state, dstate 128): persistent CTAs stream tiles through
-// a ring of shared-memory stages fed by the TMA engine's 1-D bulk copies (see ssu.cu's header
-// comment for the protocol).
+// BULK kernel of the decode step (fp32 state, dstate 128).  Persistent CTAs (as many as fit on
+// the SMs) stream tiles of `tile_rows` rows through a ring of shared-memory stages.  Warp 0 is
+// the producer: it reads the slot index of each tile ahead of time and issues a bulk
+// asynchronous copy (the TMA engine's 1-D `cp.async.bulk`) of the tile's contiguous rows into a
+// free stage, completion counted on the stage's mbarrier.  The compute warps read their rows
+// out of the stage into registers, hand the stage back at once (the producer refills it while
+// they work), update the rows, store them in place with 16-byte vector stores and write the
+// readout.  Loads in flight are bounded by shared memory (stages x tile), not by registers.
+// Every mbarrier wait is bounded in time; a timeout raises an error counter and the CTA stops
+// after its copies in flight have landed.
 #pragma once
 
 #include "ssu_device.cuh"
