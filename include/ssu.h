@@ -160,6 +160,48 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
                         ssu_stream_t stream);
 
 /*
+ * Bytes of device workspace that ssu_update_from_host needs for `shape` (a multiple of 256):
+ * dense copies of the call's indices, x, dt, B and C, each section 256-byte aligned.
+ * Returns SSU_ERR_INVALID_ARG for a NULL argument or a shape with a negative batch or a
+ * dimension below 1.
+ */
+ssu_status_t ssu_host_workspace_bytes(const ssu_shape_t *shape, int64_t *bytes);
+
+/*
+ * One decode step whose per-step operands live in HOST memory: the same step, the same
+ * arithmetic and bit-identical results as ssu_update on the same values (sglang PR #41223,
+ * Details / Kernel measurement, names the operands; a serving loop produces the indices and
+ * activations of each step on the host side of the CPU-GPU link).
+ *
+ *   state_batch_indices, x, dt, B, C   read from page-locked host memory (cudaHostAlloc or
+ *                                      cudaHostRegister), with the layouts and strides of
+ *                                      ssu_update; device or managed memory is accepted too
+ *   out                                written in page-locked host (or device) memory
+ *   state_pool, dt_bias, A, D          device memory, as for ssu_update
+ *   workspace                          caller-owned DEVICE buffer, 256-byte aligned, of at
+ *                                      least ssu_host_workspace_bytes(shape) bytes
+ *
+ * The call enqueues two kernels on `stream` and returns: the first reads the step's indices,
+ * x, dt, B and C across the link in one pass (every thread one 16-byte vector where the
+ * alignment allows) into the workspace; the second is the decode-step kernel of ssu_update,
+ * launched as a programmatic dependent of the first, reading the workspace and writing the
+ * readout straight into `out`.  No copy-engine transfer is involved.  The readout in host
+ * memory is complete once the stream reaches a point after the call (an event or a
+ * synchronisation).  The host buffers must stay unchanged, and the workspace unused by other
+ * work, until then.  Pageable host memory that is not registered is rejected with
+ * SSU_ERR_INVALID_ARG, as is device memory of another device.  Every other argument error
+ * and the run-time behaviour (skipped requests counted in the handle) are those of
+ * ssu_update.  The launch shape is the handle's forced VEC shape, else the built-in table.
+ */
+ssu_status_t ssu_update_from_host(ssu_handle_t handle, void *state_pool,
+                                  const void *state_batch_indices, const uint16_t *x,
+                                  const uint16_t *dt, const float *dt_bias, const float *A,
+                                  const uint16_t *B, const uint16_t *C, const float *D,
+                                  uint16_t *out, const ssu_shape_t *shape,
+                                  const ssu_strides_t *strides, void *workspace,
+                                  int64_t workspace_bytes, ssu_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the handle's device counters.
  * *skipped receives the number of requests skipped since the last read (may be NULL);
  * *first_bad receives the smallest skipped request index b, or -1 (may be NULL).

@@ -120,6 +120,11 @@ _EXPORTS = {
     "ssu_copy_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_copy_launch_t)]),
     "ssu_update_static": (ctypes.c_int, [_vp] * 10 + [ctypes.POINTER(ssu_shape_t),
                                                       ctypes.POINTER(ssu_strides_t), _vp, _vp]),
+    "ssu_host_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(ssu_shape_t),
+                                                ctypes.POINTER(ctypes.c_int64)]),
+    "ssu_update_from_host": (ctypes.c_int, [_vp] * 11 + [ctypes.POINTER(ssu_shape_t),
+                                                         ctypes.POINTER(ssu_strides_t), _vp,
+                                                         ctypes.c_int64, _vp]),
 }
 
 SSU_STATIC_SCRATCH_BYTES = 256
@@ -294,6 +299,38 @@ def ssu_update_static(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, 
     _check(lib().ssu_update_static(*ptrs, ctypes.byref(shape), ctypes.byref(strides),
                                    _ptr(counters_out), _stream_ptr(stream)),
            "ssu_update_static")
+
+
+def ssu_host_workspace_bytes(shape: ssu_shape_t) -> int:
+    """Device workspace bytes ``ssu_update_from_host`` needs for ``shape``."""
+    n = ctypes.c_int64()
+    _check(lib().ssu_host_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)),
+           "ssu_host_workspace_bytes")
+    return int(n.value)
+
+
+def ssu_update_from_host(handle: int, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C,
+                         D, out, workspace, stream=None) -> None:
+    """One decode step with the per-step operands (``state_batch_indices``, ``x``, ``dt``,
+    ``B``, ``C``) and ``out`` in page-locked host memory (``pin_memory()`` tensors); the state
+    pool, ``dt_bias``, ``A`` and ``D`` on the device.  ``workspace`` is a device uint8 tensor of
+    at least ``ssu_host_workspace_bytes(shape)`` bytes.  ``out`` is complete once ``stream``
+    has passed the call."""
+    shape, strides = describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)
+    ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)]
+    nbytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) \
+        else 0
+    _check(lib().ssu_update_from_host(handle, *ptrs, ctypes.byref(shape), ctypes.byref(strides),
+                                      _ptr(workspace), nbytes, _stream_ptr(stream)),
+           "ssu_update_from_host")
+
+
+def ssu_update_from_host_raw(handle: int, ptrs, shape: ssu_shape_t, strides: ssu_strides_t,
+                             workspace: int, workspace_bytes: int, stream: int | None) -> int:
+    """ssu_update_from_host with precomputed pointers/structs; returns the status."""
+    return int(lib().ssu_update_from_host(handle, *ptrs, ctypes.byref(shape),
+                                          ctypes.byref(strides), workspace, workspace_bytes,
+                                          stream))
 
 
 def ssu_update_raw(handle: int, ptrs, shape: ssu_shape_t, strides: ssu_strides_t,

@@ -26,6 +26,7 @@
 #include "ssu.h"
 #include "ssu_bulk.cuh"
 #include "ssu_device.cuh"
+#include "ssu_stage.cuh"
 #include "ssu_vec.cuh"
 #include "ssu_host.h"
 
@@ -81,6 +82,51 @@ bool bulk_fits(const ssu_handle_s &hd, const ssu_launch_t &l, const ssu_shape_t 
     if (st->state[2] != kDstate) return false;
     const int tile_rows = l.rows_per_warp * l.warps_per_cta;
     return static_cast<int>(bulk_smem_bytes(l.stages, tile_rows)) <= hd.smem_optin;
+}
+
+// The kernels' parameter block for one call (validated arguments, element strides).
+SsuParams make_params(void *state_pool, const void *idx, const uint16_t *x, const uint16_t *dt,
+                      const float *dt_bias, const float *A, const uint16_t *B, const uint16_t *C,
+                      const float *D, uint16_t *out, const ssu_shape_t &s,
+                      const ssu_strides_t *strides, long long slabs, int rows_per_tile,
+                      unsigned *err) {
+    SsuParams p;
+    p.state = state_pool;
+    p.idx = idx;
+    p.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    p.dt = reinterpret_cast<const __nv_bfloat16 *>(dt);
+    p.dt_bias = dt_bias;
+    p.A = A;
+    p.B = reinterpret_cast<const __nv_bfloat16 *>(B);
+    p.C = reinterpret_cast<const __nv_bfloat16 *>(C);
+    p.D = D;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.st_pool = strides->state[0];
+    p.st_head = strides->state[1];
+    p.st_row = strides->state[2];
+    p.x_b = strides->x[0];
+    p.x_h = strides->x[1];
+    p.out_b = strides->out[0];
+    p.out_h = strides->out[1];
+    p.dt_b = strides->dt[0];
+    p.dt_h = strides->dt[1];
+    p.B_b = strides->B[0];
+    p.B_g = strides->B[1];
+    p.C_b = strides->C[0];
+    p.C_g = strides->C[1];
+    p.bias_h = strides->dt_bias[0];
+    p.D_h = strides->D[0];
+    p.A_h = strides->A[0];
+    p.idx_s = strides->idx;
+    p.pool_size = s.pool_size;
+    p.batch = s.batch;
+    p.nheads = static_cast<int>(s.nheads);
+    p.headdim = static_cast<int>(s.headdim);
+    p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
+    p.slabs = static_cast<int>(slabs);
+    p.rows_per_cta = rows_per_tile;
+    p.err = err;
+    return p;
 }
 
 }  // namespace
@@ -201,42 +247,8 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
     if (tiles > INT_MAX)
         return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
 
-    SsuParams p;
-    p.state = state_pool;
-    p.idx = state_batch_indices;
-    p.x = reinterpret_cast<const __nv_bfloat16 *>(x);
-    p.dt = reinterpret_cast<const __nv_bfloat16 *>(dt);
-    p.dt_bias = dt_bias;
-    p.A = A;
-    p.B = reinterpret_cast<const __nv_bfloat16 *>(B);
-    p.C = reinterpret_cast<const __nv_bfloat16 *>(C);
-    p.D = D;
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.st_pool = strides->state[0];
-    p.st_head = strides->state[1];
-    p.st_row = strides->state[2];
-    p.x_b = strides->x[0];
-    p.x_h = strides->x[1];
-    p.out_b = strides->out[0];
-    p.out_h = strides->out[1];
-    p.dt_b = strides->dt[0];
-    p.dt_h = strides->dt[1];
-    p.B_b = strides->B[0];
-    p.B_g = strides->B[1];
-    p.C_b = strides->C[0];
-    p.C_g = strides->C[1];
-    p.bias_h = strides->dt_bias[0];
-    p.D_h = strides->D[0];
-    p.A_h = strides->A[0];
-    p.idx_s = strides->idx;
-    p.pool_size = s.pool_size;
-    p.batch = s.batch;
-    p.nheads = static_cast<int>(s.nheads);
-    p.headdim = static_cast<int>(s.headdim);
-    p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
-    p.slabs = static_cast<int>(slabs);
-    p.rows_per_cta = rows_per_tile;
-    p.err = handle->err;
+    const SsuParams p = make_params(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
+                                    out, s, strides, slabs, rows_per_tile, handle->err);
 
     DeviceGuard guard(handle->device);
     if (guard.err != cudaSuccess)
@@ -287,6 +299,166 @@ ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *s
                     host[2]);
     if (host[0]) return fail(SSU_ERR_INDEX_OOB, "%u request(s) named a slot outside the pool",
                              host[0]);
+    return ok();
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Per-step operands in host memory: a staging kernel, then the decode-step kernel.
+
+namespace {
+
+long long round256(long long v) { return (v + 255) & ~255LL; }
+
+// Byte offsets of the dense staged operands in the workspace.
+struct HostLayout {
+    long long idx, x, dt, B, C, total;
+};
+
+HostLayout host_layout(const ssu_shape_t &s) {
+    const long long esz = s.index_dtype == SSU_INDEX_I64 ? 8 : 4;
+    const long long bc = round256(s.batch * s.ngroups * s.dstate * 2);
+    HostLayout L;
+    L.idx = 0;
+    L.x = round256(s.batch * esz);
+    L.dt = L.x + round256(s.batch * s.nheads * s.headdim * 2);
+    L.B = L.dt + round256(s.batch * s.nheads * 2);
+    L.C = L.B + bc;
+    L.total = L.C + bc;
+    return L;
+}
+
+// The address through which kernels on the current device reach operand `p`: the device
+// mapping of page-locked host memory, or the pointer itself for device memory of this device
+// and for managed memory.
+ssu_status_t device_view(const void *p, const char *name, int dev, const void **view) {
+    cudaPointerAttributes a;
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SSU_ERR_CUDA, "cudaPointerGetAttributes(%s): %s", name,
+                    cudaGetErrorString(e));
+    }
+    if (a.type == cudaMemoryTypeHost) {
+        if (!a.devicePointer)
+            return fail(SSU_ERR_INVALID_ARG, "%s: page-locked memory not mapped on device %d",
+                        name, dev);
+        *view = a.devicePointer;
+        return SSU_OK;
+    }
+    if (a.type == cudaMemoryTypeManaged || (a.type == cudaMemoryTypeDevice && a.device == dev)) {
+        *view = p;
+        return SSU_OK;
+    }
+    if (a.type == cudaMemoryTypeDevice)
+        return fail(SSU_ERR_INVALID_ARG, "%s is memory of device %d, not %d", name, a.device,
+                    dev);
+    return fail(SSU_ERR_INVALID_ARG,
+                "%s is pageable host memory: allocate it with cudaHostAlloc or register it "
+                "with cudaHostRegister",
+                name);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssu_status_t ssu_host_workspace_bytes(const ssu_shape_t *shape, int64_t *bytes) {
+    if (!shape || !bytes) return fail(SSU_ERR_INVALID_ARG, "NULL argument");
+    const ssu_shape_t &s = *shape;
+    if (s.batch < 0 || s.nheads < 1 || s.headdim < 1 || s.dstate < 1 || s.ngroups < 1)
+        return fail(SSU_ERR_INVALID_ARG, "batch must be >= 0 and every dimension >= 1");
+    *bytes = host_layout(s).total;
+    return ok();
+}
+
+ssu_status_t ssu_update_from_host(ssu_handle_t handle, void *state_pool,
+                                  const void *state_batch_indices, const uint16_t *x,
+                                  const uint16_t *dt, const float *dt_bias, const float *A,
+                                  const uint16_t *B, const uint16_t *C, const float *D,
+                                  uint16_t *out, const ssu_shape_t *shape,
+                                  const ssu_strides_t *strides, void *workspace,
+                                  int64_t workspace_bytes, ssu_stream_t stream) {
+    if (!handle) return fail(SSU_ERR_INVALID_ARG, "NULL handle");
+    ssu_status_t st = validate_impl(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C,
+                                    D, out, shape, strides);
+    if (st != SSU_OK || shape->batch == 0) return st;
+    const ssu_shape_t &s = *shape;
+    const HostLayout L = host_layout(s);
+    if (!workspace) return fail(SSU_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned(workspace, 256))
+        return fail(SSU_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    if (workspace_bytes < L.total)
+        return fail(SSU_ERR_INVALID_ARG, "workspace holds %lld bytes; this shape needs %lld",
+                    (long long)workspace_bytes, L.total);
+    ssu_launch_t l = handle->has_override && handle->override_launch.mode == SSU_MODE_VEC
+                         ? handle->override_launch
+                         : table_launch(*handle, s, strides);
+    if (l.rows_per_warp == 16 && (s.state_dtype != SSU_STATE_F32 || s.dstate != 128))
+        return fail(SSU_ERR_UNSUPPORTED, "16 rows per warp needs an fp32 state of dstate 128");
+    const int rows_per_tile = l.rows_per_warp * l.warps_per_cta;
+    const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
+    const long long tiles = s.batch * s.nheads * slabs;
+    if (tiles > INT_MAX) return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
+
+    DeviceGuard guard(handle->device);
+    if (guard.err != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
+    const void *v_idx, *v_x, *v_dt, *v_B, *v_C, *v_out;
+    if ((st = device_view(state_batch_indices, "state_batch_indices", handle->device, &v_idx)) ||
+        (st = device_view(x, "x", handle->device, &v_x)) ||
+        (st = device_view(dt, "dt", handle->device, &v_dt)) ||
+        (st = device_view(B, "B", handle->device, &v_B)) ||
+        (st = device_view(C, "C", handle->device, &v_C)) ||
+        (st = device_view(out, "out", handle->device, &v_out)))
+        return st;
+
+    // Dense staged copies: idx [bs], x [bs,H,P], dt [bs,H], B and C [bs,G,N].
+    char *ws = static_cast<char *>(workspace);
+    const long long esz = s.index_dtype == SSU_INDEX_I64 ? 8 : 4;
+    const ssu_strides_t &u = *strides;
+    StageParams q;
+    long long chunk0 = 0;
+    q.job[0] = stage_job(v_idx, ws + L.idx, s.batch, 1, u.idx * esz, 0, esz, chunk0);
+    q.job[1] = stage_job(v_x, ws + L.x, s.batch, s.nheads, u.x[0] * 2, u.x[1] * 2,
+                         s.headdim * 2, chunk0);
+    q.job[2] = stage_job(v_dt, ws + L.dt, s.batch, s.nheads, u.dt[0] * 2, u.dt[1] * 2, 2, chunk0);
+    q.job[3] = stage_job(v_B, ws + L.B, s.batch, s.ngroups, u.B[0] * 2, u.B[1] * 2,
+                         s.dstate * 2, chunk0);
+    q.job[4] = stage_job(v_C, ws + L.C, s.batch, s.ngroups, u.C[0] * 2, u.C[1] * 2,
+                         s.dstate * 2, chunk0);
+    q.njobs = kStageJobs;
+    q.total = chunk0;
+
+    ssu_strides_t dense = u;
+    dense.idx = 1;
+    const int64_t x_dense[3] = {s.nheads * s.headdim, s.headdim, 1};
+    const int64_t dt_dense[3] = {s.nheads, 1, 0};
+    const int64_t bc_dense[3] = {s.ngroups * s.dstate, s.dstate, 1};
+    for (int i = 0; i < 3; ++i) {
+        dense.x[i] = x_dense[i];
+        dense.dt[i] = dt_dense[i];
+        dense.B[i] = bc_dense[i];
+        dense.C[i] = bc_dense[i];
+    }
+    auto bf = [](const char *ptr) { return reinterpret_cast<const uint16_t *>(ptr); };
+    const SsuParams p =
+        make_params(state_pool, ws + L.idx, bf(ws + L.x), bf(ws + L.dt), dt_bias, A,
+                    bf(ws + L.B), bf(ws + L.C), D,
+                    const_cast<uint16_t *>(static_cast<const uint16_t *>(v_out)), s, &dense,
+                    slabs, rows_per_tile, handle->err);
+
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_stage(q, handle->sm_count, handle->pdl, cs);
+    if (e == cudaSuccess)
+        e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16,
+                       s.index_dtype == SSU_INDEX_I64, l.rows_per_warp, l.warps_per_cta,
+                       dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
+                            static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535)),
+                       true, cs);
+    if (e != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "ssu_update_from_host: %s", cudaGetErrorString(e));
     return ok();
 }
 
@@ -364,42 +536,8 @@ extern "C" ssu_status_t ssu_update_static(void *state_pool, const void *state_ba
     const long long tiles = s.batch * s.nheads * slabs;
     if (tiles > INT_MAX) return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
 
-    SsuParams p;
-    p.state = state_pool;
-    p.idx = state_batch_indices;
-    p.x = reinterpret_cast<const __nv_bfloat16 *>(x);
-    p.dt = reinterpret_cast<const __nv_bfloat16 *>(dt);
-    p.dt_bias = dt_bias;
-    p.A = A;
-    p.B = reinterpret_cast<const __nv_bfloat16 *>(B);
-    p.C = reinterpret_cast<const __nv_bfloat16 *>(C);
-    p.D = D;
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.st_pool = strides->state[0];
-    p.st_head = strides->state[1];
-    p.st_row = strides->state[2];
-    p.x_b = strides->x[0];
-    p.x_h = strides->x[1];
-    p.out_b = strides->out[0];
-    p.out_h = strides->out[1];
-    p.dt_b = strides->dt[0];
-    p.dt_h = strides->dt[1];
-    p.B_b = strides->B[0];
-    p.B_g = strides->B[1];
-    p.C_b = strides->C[0];
-    p.C_g = strides->C[1];
-    p.bias_h = strides->dt_bias[0];
-    p.D_h = strides->D[0];
-    p.A_h = strides->A[0];
-    p.idx_s = strides->idx;
-    p.pool_size = s.pool_size;
-    p.batch = s.batch;
-    p.nheads = static_cast<int>(s.nheads);
-    p.headdim = static_cast<int>(s.headdim);
-    p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
-    p.slabs = static_cast<int>(slabs);
-    p.rows_per_cta = rows_per_tile;
-    p.err = scratch;
+    const SsuParams p = make_params(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
+                                    out, s, strides, slabs, rows_per_tile, scratch);
 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     // The counters start every call at {0 skipped, no smallest index (all ones), 0 timeouts}.

@@ -216,3 +216,38 @@ def test_check_indices_finds_repeats_and_out_of_range(ssu):
     assert ssu.ssu_check_indices(neg, 1000) == 9
     assert ssu.ssu_check_indices(torch.zeros(0, dtype=torch.int32), 0) == -1
     assert ssu.ssu_check_indices(rep, 1000) == 200 and "repeats slot" in ssu.last_error()
+
+
+# ---- host-operand entry point: workspace size and the checks made before any CUDA call ----
+
+def test_host_workspace_bytes_closed_form(ssu):
+    """Dense idx, x, dt, B, C sections, each rounded up to 256 bytes."""
+    r = lambda v: (v + 255) // 256 * 256
+    for bs, H, P, N, G, i64 in ((128, 16, 64, 128, 1, False), (3, 5, 7, 64, 1, True),
+                                (1, 4, 3, 256, 2, False), (0, 16, 64, 128, 1, False)):
+        shape = ssu.ssu_shape_t(bs, H, P, N, G, bs + 1, 1 if i64 else 0, 0)
+        want = (r(bs * (8 if i64 else 4)) + r(bs * H * P * 2) + r(bs * H * 2)
+                + 2 * r(bs * G * N * 2))
+        assert ssu.ssu_host_workspace_bytes(shape) == want
+    # batch 128, 16 heads: exactly the step's 332,288 input bytes (every section a multiple
+    # of 256 already)
+    assert ssu.ssu_host_workspace_bytes(ssu.ssu_shape_t(128, 16, 64, 128, 1, 129, 0, 0)) == \
+        128 * 4 + 128 * (16 * 64 + 256) * 2 + 128 * 16 * 2
+
+
+def test_host_workspace_bytes_rejects_bad_shapes(ssu):
+    n = ctypes.c_int64()
+    assert ssu.lib().ssu_host_workspace_bytes(None, ctypes.byref(n)) == ssu.SSU_ERR_INVALID_ARG
+    for bad in (dict(batch=-1), dict(nheads=0), dict(dstate=0)):
+        shape = ssu.ssu_shape_t(8, 16, 64, 128, 1, 9, 0, 0)
+        for k, v in bad.items():
+            setattr(shape, k, v)
+        assert ssu.lib().ssu_host_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)) == \
+            ssu.SSU_ERR_INVALID_ARG
+
+
+def test_host_entry_rejects_null_handle_and_invalid_operands(ssu):
+    ptrs, shape, st = canonical()
+    f = ssu.ssu_update_from_host_raw
+    assert f(None, ptrs, shape, st, BASE, 1 << 20, None) == ssu.SSU_ERR_INVALID_ARG
+    assert "handle" in ssu.last_error()
