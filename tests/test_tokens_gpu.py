@@ -173,3 +173,37 @@ def test_tokens_serving_batch_128_sampled(op):
     keep = torch.from_numpy(np.nonzero(mask)[0]).cuda()
     assert torch.equal(pool_d[keep], torch.from_numpy(pool[mask]).cuda())
 
+
+
+@pytest.mark.parametrize("T,N", [(2, 128), (5, 128), (3, 64), (4, 256)])
+def test_unaligned_B_C_take_the_scalar_loads_with_the_same_bits(op, T, N):
+    """B and C one element past an 8-byte boundary (only 2-byte aligned) cannot be read as
+    column vectors; the kernel then loads them element by element.  Both forms must give the
+    same bits, with the 2-token (T <= 2) and the 4-token (T >= 3) prefetch rings."""
+    bs, H = 10, 8
+    pr, x, dt, B, C = _tokens_problem(bs, T, H=H, N=N, seed=T + N)
+    aligned_pool, aligned_out, aligned_inter = _run(op, pr, x, dt, B, C)
+    dev = to_device(pr, "cuda")
+    out = torch.zeros(bs, T, H, 64, dtype=torch.bfloat16, device="cuda")
+    inter = torch.full((bs, T, H, 64, N), 123.0, device="cuda")
+    # [bs, T, 1, N] views at element offset 1 of a wider buffer: 2-byte alignment only
+    width = 2 * N + 3
+    buf = torch.zeros(bs, T, width, dtype=torch.bfloat16, device="cuda")
+    buf[:, :, 1:1 + N] = bf16_tensor(B, "cuda")[:, :, 0]
+    buf[:, :, 2 + N:2 + 2 * N] = bf16_tensor(C, "cuda")[:, :, 0]
+    Bv = buf[:, :, 1:1 + N].unsqueeze(2)
+    Cv = buf[:, :, 2 + N:2 + 2 * N].unsqueeze(2)
+    assert Bv.data_ptr() % 8 != 0
+    op.tokens(dev["state_pool"], dev["state_batch_indices"], bf16_tensor(x, "cuda"),
+              bf16_tensor(dt, "cuda"), dev["dt_bias"], dev["A"], Bv, Cv, dev["D"], out, inter)
+    torch.cuda.synchronize()
+    assert np.array_equal(dev["state_pool"].cpu().numpy(), aligned_pool)
+    assert np.array_equal(bits_of(out), aligned_out)
+    assert np.array_equal(inter.cpu().numpy(), aligned_inter)
+
+
+def test_long_token_runs_cross_the_per_warp_scalar_batches(op):
+    """dt and dA are computed 32 tokens at a time (one per lane); 40 tokens cross a batch."""
+    pr, x, dt, B, C = _tokens_problem(3, 40, H=4, seed=21)
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C)
+    _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter)
