@@ -353,7 +353,7 @@ def time_e2e(wl_, handle, steps: int, dev) -> dict:
             step(i % wl_.n_sets)
     g.replay()
     stream.synchronize()
-    reps = max(1, steps // per_graph)
+    reps = max(10, steps // per_graph)
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for _ in range(reps):
@@ -854,6 +854,21 @@ def bytes_per_call_tokens(bs: int, T: int, intermediate: bool, H: int = NHEADS,
     return state + T * per_token + bs * 4 + 3 * H * 4 + inter
 
 
+def run_e2e_only(args) -> None:
+    """The e2e object alone (host-buffer paths) for the chosen batch, 16 heads."""
+    import torch
+
+    import selective_state_update_02_gb300 as ssu
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = ssu.ssu_create(0)
+    w = Workload(args.batch, NHEADS, dev, seed=5, l2_bytes=l2, packed=True)
+    e2e = time_e2e(w, handle, args.e2e_steps, dev)
+    print(json.dumps({"batch": args.batch, "e2e": e2e}), flush=True)
+    assert ssu.ssu_get_error(handle) == (0, -1)
+    ssu.ssu_destroy(handle)
+
+
 def run_tokens(args) -> None:
     """Multi-token step at batch 128 (cold-L2 rotation): µs per call and GB/s for T = 1..4,
     with and without the intermediate-state output."""
@@ -869,7 +884,7 @@ def run_tokens(args) -> None:
     rng = np.random.default_rng(9)
     peaks = load_peaks()
     shapes = [None]
-    tokens_list = (1, 2, 3, 4)
+    tokens_list = tuple(args.tokens_list)
     if args.sweep:
         shapes = [(r, w) for r in (4, 8, 16) for w in (1, 2, 4)]
         tokens_list = (2, 4)
@@ -987,6 +1002,10 @@ def main() -> None:
     ap.add_argument("--sweep", action="store_true", help="launch-shape sweep instead")
     ap.add_argument("--calibrate", action="store_true",
                     help="library copy / in-place rates at the call sizes instead")
+    ap.add_argument("--tokens-list", type=int, nargs="+", default=[1, 2, 3, 4],
+                    help="token counts timed by --tokens")
+    ap.add_argument("--e2e-only", action="store_true",
+                    help="only the host-buffer (e2e) measurements at the chosen batch")
     ap.add_argument("--skip-ceiling", action="store_true",
                     help="skip the same-size in-place ceiling measurement")
     ap.add_argument("--sweep-batches", type=int, nargs="+", default=[8, 128, 512])
@@ -1005,6 +1024,8 @@ def main() -> None:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
+    elif args.e2e_only:
+        run_e2e_only(args)
     else:
         run_ours(args)
 

@@ -112,20 +112,16 @@ __device__ __forceinline__ void load_pairs(const unsigned short *p, unsigned (&w
     }
 }
 
-template <int RPW, int NC, bool VEC>
-__device__ __forceinline__ void load_token(const TokenParams &q, long long b, int h, int g,
-                                           int row0, int t, int lane, TokenBits<NC> &in) {
-    const SsuParams &p = q.p;
-    load_pairs<NC, VEC>(reinterpret_cast<const unsigned short *>(p.B) + b * p.B_b + t * q.B_t +
-                            g * p.B_g + lane_offset<NC>(lane),
-                        in.b);
-    load_pairs<NC, VEC>(reinterpret_cast<const unsigned short *>(p.C) + b * p.C_b + t * q.C_t +
-                            g * p.C_g + lane_offset<NC>(lane),
-                        in.c);
-    in.x = (lane < RPW && row0 + lane < p.headdim)
-               ? reinterpret_cast<const unsigned short *>(p.x)[b * p.x_b + t * q.x_t +
-                                                               h * p.x_h + row0 + lane]
-               : static_cast<unsigned short>(0);
+// One token's inputs into a ring slot: `B` and `C` point at the lane's first column of the
+// token's rows, `x` at the lane's x element (read only where `x_live`: lanes r < RPW whose row
+// exists).
+template <int NC, bool VEC>
+__device__ __forceinline__ void load_token(const unsigned short *B, const unsigned short *C,
+                                           const unsigned short *x, bool x_live,
+                                           TokenBits<NC> &in) {
+    load_pairs<NC, VEC>(B, in.b);
+    load_pairs<NC, VEC>(C, in.c);
+    in.x = x_live ? *x : static_cast<unsigned short>(0);
 }
 
 // dt and dA of token base + lane (lanes past the last token hold 0): each token's softplus
@@ -147,7 +143,10 @@ __device__ __forceinline__ void token_scalars(const TokenParams &q, long long b,
     }
 }
 
-// The T-token loop of one warp over its RPW rows held in v (see the kernel below).
+// The T-token loop of one warp over its RPW rows held in v (see the kernel below).  The
+// per-token inputs are read through pointers built once per warp and advanced by one token
+// stride per token; the outputs' addresses are formed per token (carrying output pointers
+// through the loop as well measured 5-10 % slower once the ring refills).
 template <int RPW, int NC, typename ST, bool VEC, int PD>
 __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW][NC], long long b,
                                            int h, int row0, int lane) {
@@ -156,11 +155,23 @@ __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW]
     const float Ah = p.A[h * p.A_h];
     const float Dh = p.D[h * p.D_h];
     const int g = h / p.heads_per_group;
+    const int lo = lane_offset<NC>(lane);
+    const unsigned short *Bn = reinterpret_cast<const unsigned short *>(p.B) + b * p.B_b +
+                               g * p.B_g + lo;
+    const unsigned short *Cn = reinterpret_cast<const unsigned short *>(p.C) + b * p.C_b +
+                               g * p.C_g + lo;
+    const bool x_live = lane < RPW && row0 + lane < p.headdim;
+    const unsigned short *xn = reinterpret_cast<const unsigned short *>(p.x) + b * p.x_b +
+                               h * p.x_h + row0 + (x_live ? lane : 0);
     // A ring of the next PD tokens' inputs, unrolled so every slot is a fixed register.
     TokenBits<NC> ring[PD];
 #pragma unroll
     for (int k = 0; k < PD; ++k)
-        if (k < q.tokens) load_token<RPW, NC, VEC>(q, b, h, g, row0, k, lane, ring[k]);
+        if (k < q.tokens)
+            load_token<NC, VEC>(Bn + k * q.B_t, Cn + k * q.C_t, xn + k * q.x_t, x_live, ring[k]);
+    Bn += PD * q.B_t;  // now token PD's
+    Cn += PD * q.C_t;
+    xn += PD * q.x_t;
     float lane_dtv, lane_dA;
     token_scalars(q, b, h, bias, Ah, 0, lane, lane_dtv, lane_dA);
     for (int t0 = 0; t0 < q.tokens; t0 += PD) {
@@ -175,16 +186,19 @@ __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW]
             widen_pairs<NC>(ring[k].b, bb);
             widen_pairs<NC>(ring[k].c, cc);
             const float xl = widen_bf16(ring[k].x);
-            if (t + PD < q.tokens) load_token<RPW, NC, VEC>(q, b, h, g, row0, t + PD, lane, ring[k]);
+            if (t + PD < q.tokens) load_token<NC, VEC>(Bn, Cn, xn, x_live, ring[k]);
+            Bn += q.B_t;
+            Cn += q.C_t;
+            xn += q.x_t;
+            const float kl = dtv * xl;  // lane r < RPW: dt * x of row r
             float part[RPW];
 #pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                const float xr = __shfl_sync(0xffffffffu, xl, r);
-                part[r] = update_lane_packed<NC>(v[r], dA, dtv * xr, bb, cc);
-            }
+            for (int r = 0; r < RPW; ++r)
+                part[r] = update_lane_packed<NC>(v[r], dA, __shfl_sync(0xffffffffu, kl, r), bb,
+                                                 cc);
             if (q.inter) {
                 ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
-                           row0 * q.in_p + lane_offset<NC>(lane);
+                           row0 * q.in_p + lo;
 #pragma unroll
                 for (int r = 0; r < RPW; ++r)
                     if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, v[r]);
