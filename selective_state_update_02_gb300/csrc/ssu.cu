@@ -60,12 +60,13 @@ namespace {
 
 // Built-in launch-shape table, from the cold-L2 sweeps on GB300 (bench.py --sweep, with and
 // without --dstate / --state-dtype).  The VEC kernel with 8 rows per warp and 2 warps per CTA
-// is fastest from batch 32 up (dstate 256: 4 rows per warp, fewer registers).  A call too
-// small to give every SM 16 warps at that size steps down to 4, then 2 rows per warp with 4
-// warps per CTA (batch 8: 3.80 us instead of 3.97).  The tile never exceeds the headdim.
+// is fastest from batch 32 up (an fp32 state at dstate 256: 4 rows per warp, fewer
+// registers; 16 rows per warp is slower in every bucket).  A call too small to give every SM
+// 16 warps at that size steps down to 4, then 2 rows per warp with 4 warps per CTA (batch 8:
+// 3.80 us instead of 3.97).  The tile never exceeds the headdim.
 ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
     (void)st;
-    int rpw = s.dstate == 256 ? 4 : 8;
+    int rpw = s.dstate == 256 && s.state_dtype == SSU_STATE_F32 ? 4 : 8;
     const long long rows = s.batch * s.nheads * s.headdim;
     while (rpw > 2 && rows / rpw < 16LL * hd.sm_count) rpw >>= 1;
     while (rpw > 1 && rpw > s.headdim) rpw >>= 1;

@@ -6,7 +6,9 @@
  * The case is the hand-computed one of the oracle's pins, widened to dstate 64 with zero
  * columns: S = [1, 2, 0, ...], x = 1, dt = dt_bias = 0, A = -1, B = [1, -1, 0, ...],
  * C = [1, 1, 0, ...], D = 0.5, so dtv = ln 2, dA = 1/2, S' = [0.5 + ln 2, 1 - ln 2, 0, ...] and
- * y = 2 exactly (bf16 0x4000).  A second pool slot must stay untouched.
+ * y = 2 exactly (bf16 0x4000).  A second pool slot must stay untouched.  The step then runs
+ * again from the same pool through ssu_update_from_host with the per-step operands and the
+ * readout in page-locked host memory, and must give the same bits.
  *
  * Exit status 0 and "ok" on success; "no-device" (status 0) when no GPU is present, after the
  * host-side checks; a message and status 1 otherwise.
@@ -125,6 +127,47 @@ int main(void) {
     float got[2 * N];
     cudaMemcpy(&y, d_out, 2, cudaMemcpyDeviceToHost);
     cudaMemcpy(got, d_pool, sizeof got, cudaMemcpyDeviceToHost);
+
+    /* The same step with the per-step operands and the readout in page-locked host memory
+       (ssu_update_from_host), from the original pool: the same bits. */
+    {
+        int *h_idx;
+        uint16_t *h_x, *h_dt, *h_B, *h_C, *h_out;
+        void *d_ws;
+        int64_t ws_bytes = 0;
+        if (cudaHostAlloc((void **)&h_idx, 4, cudaHostAllocDefault) ||
+            cudaHostAlloc((void **)&h_x, 2, cudaHostAllocDefault) ||
+            cudaHostAlloc((void **)&h_dt, 2, cudaHostAllocDefault) ||
+            cudaHostAlloc((void **)&h_B, sizeof B, cudaHostAllocDefault) ||
+            cudaHostAlloc((void **)&h_C, sizeof C, cudaHostAllocDefault) ||
+            cudaHostAlloc((void **)&h_out, 2, cudaHostAllocDefault))
+            return fail("cudaHostAlloc");
+        *h_idx = idx, *h_x = x, *h_dt = dt, *h_out = 0xFFFF;
+        memcpy(h_B, B, sizeof B);
+        memcpy(h_C, C, sizeof C);
+        if (ssu_host_workspace_bytes(&shape, &ws_bytes) != SSU_OK || ws_bytes < 256)
+            return fail("workspace size");
+        if (cudaMalloc(&d_ws, (size_t)ws_bytes)) return fail("cudaMalloc workspace");
+        float *d_pool2;
+        if (cudaMalloc((void **)&d_pool2, sizeof pool)) return fail("cudaMalloc pool");
+        cudaMemcpy(d_pool2, pool, sizeof pool, cudaMemcpyHostToDevice);
+        /* pageable host memory is refused before anything is enqueued */
+        if (ssu_update_from_host(h, d_pool2, h_idx, h_x, h_dt, d_bias, d_A, B, h_C, d_D, h_out,
+                                 &shape, &st, d_ws, ws_bytes, NULL) != SSU_ERR_INVALID_ARG)
+            return fail("pageable B must be refused");
+        if (ssu_update_from_host(h, d_pool2, h_idx, h_x, h_dt, d_bias, d_A, h_B, h_C, d_D, h_out,
+                                 &shape, &st, d_ws, ws_bytes, NULL) != SSU_OK)
+            return fail("update_from_host");
+        if (cudaStreamSynchronize(NULL) != cudaSuccess) return fail("synchronize");
+        float got2[2 * N];
+        cudaMemcpy(got2, d_pool2, sizeof got2, cudaMemcpyDeviceToHost);
+        if (*h_out != y) return fail("host-path readout differs");
+        if (memcmp(got2, got, sizeof got) != 0) return fail("host-path state differs");
+        cudaFree(d_pool2);
+        cudaFree(d_ws);
+        cudaFreeHost(h_idx), cudaFreeHost(h_x), cudaFreeHost(h_dt);
+        cudaFreeHost(h_B), cudaFreeHost(h_C), cudaFreeHost(h_out);
+    }
     ssu_destroy(h);
 
     const double ln2 = log(2.0);
