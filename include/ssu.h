@@ -13,11 +13,13 @@
  *     S[p,n]   = S[p,n] * dA + (dtv * x[b,h,p]) * B[b,g,n]  in place in state_pool[s,h]
  *     out[b,h,p] = bf16_rne( sum_n S[p,n] * C[b,g,n] + D[h] * x[b,h,p] )
  *
- * Types.  The state pool is fp32 or bf16 (ssu_shape_t.state_dtype; either way the update runs in
- * fp32 and a bf16 state is rounded to nearest even when stored).  x, dt, B, C and out are
- * bfloat16, passed as uint16_t pointers to their bit patterns.  dt_bias, A and D are fp32.  state_batch_indices is int32
- * or int64 (ssu_shape_t.index_dtype).  All data pointers are DEVICE pointers on the handle's
- * device; the caller owns every buffer.  Sizes and strides are in ELEMENTS (not bytes).
+ * Types.  The state pool is fp32 or bf16 (ssu_shape_t.state_dtype; either way the update runs
+ * in fp32 and a bf16 state is rounded to nearest even when stored).  x, dt, B, C and out are
+ * bfloat16, passed as uint16_t pointers to their bit patterns.  dt_bias, A and D are fp32.
+ * state_batch_indices is int32 or int64 (ssu_shape_t.index_dtype).  All data pointers are
+ * DEVICE pointers on the handle's device (ssu_update_from_host alone takes its per-step
+ * operands and readout in page-locked host memory); the caller owns every buffer.  Sizes and
+ * strides are in ELEMENTS (not bytes).
  *
  * Streams and asynchrony.  ssu_update validates on the host, then enqueues one kernel on
  * `stream` and returns.  It allocates nothing, copies nothing and never synchronises, so it
@@ -28,7 +30,8 @@
  * (thread-local).  A request whose slot lies outside [0, pool_size) is skipped on the device
  * (its slot and its out rows are not touched) and counted; ssu_get_error reports the count.
  * Duplicate slots within one call are a precondition violation (two requests would update
- * the same state concurrently); they are not detected.
+ * the same state concurrently); they are not detected.  So is any overlap between what a
+ * call writes (the named state slots, out, intermediate states) and what it only reads.
  *
  * Threading.  A handle may be used from one host thread at a time.  Calls on different
  * handles are independent.
@@ -272,8 +275,10 @@ typedef struct {
  * T consecutive decode steps (1 <= T <= SSU_MAX_TOKENS).  Pointers, shape and ssu_strides_t as
  * for ssu_update (describing token 0), plus `tokens` = T, the token strides, and
  * `intermediate` (device buffer of the state's dtype, 16-byte aligned, or NULL for none).
- * Within a call the running state stays in fp32; a bf16 state is rounded only when written.  Same error behaviour as
- * ssu_update; enqueued on `stream`; allocates and synchronises nothing.
+ * Within a call the running state stays in fp32; a bf16 state is rounded only when written.
+ * Same error behaviour as ssu_update; enqueued on `stream`; allocates and synchronises
+ * nothing.  B and C are read as whole 4- or 8-byte column groups when their base and strides
+ * allow it, element by element otherwise (same results either way).
  */
 ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                                const void *state_batch_indices, const uint16_t *x,

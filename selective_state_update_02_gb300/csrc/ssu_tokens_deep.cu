@@ -1,6 +1,6 @@
 // Multi-token decode-step kernels with a prefetch ring of 4 tokens (used from 3 tokens per
-// call on, up to dstate 128), compiled apart from ssu_tokens.cu so the two sets of instantiations build in
-// parallel.
+// call on, up to dstate 128), compiled apart from ssu_tokens.cu so the two sets of
+// instantiations build in parallel.
 
 #include <cstring>
 
