@@ -130,13 +130,18 @@ def test_tokens(op, N, dtype):
         check_y(outb[:, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, N, f"y token {t}")
 
 
-def test_bf16_state_serving_batch_128_sampled(op):
-    bs, H = 128, 16
-    rng = np.random.default_rng(5)
-    pool = wl.state_pool(rng, 2432, H, dtype="bf16")
-    idx = wl.rotation_sets(bs, 19, seed=5)[7]
+@pytest.mark.parametrize("N,dtype", [(128, "bf16"), (64, "f32"), (256, "f32"), (256, "bf16"),
+                                     (64, "bf16")])
+def test_serving_batch_128_sampled(op, N, dtype):
+    """Each bucket at the batch the bench times it (128 requests, 16 heads, the built-in
+    launch table), slots scattered over a 384-slot pool; sampled requests against the oracle,
+    every other slot unchanged."""
+    bs, H, slots = 128, 16, 384
+    rng = np.random.default_rng(5 + N)
+    pool = wl.state_pool(rng, slots, H, N=N, dtype=dtype)
+    idx = wl.rotation_sets(bs, 3, seed=5)[1]
     dt_bias, A, D = wl.head_params(rng, H)
-    x, dt, B, C = wl.request_inputs(rng, bs, H)
+    x, dt, B, C = wl.request_inputs(rng, bs, H, N=N)
     pool_d = pool_tensor(pool, "cuda")
     out = torch.zeros(bs, H, 64, dtype=torch.bfloat16, device="cuda")
     op(pool_d, torch.from_numpy(idx).cuda(), bf16_tensor(x, "cuda"), bf16_tensor(dt, "cuda"),
@@ -148,7 +153,7 @@ def test_bf16_state_serving_batch_128_sampled(op):
     got = pool_host(pool_d)
     check_state(got[idx[rows]], ref_states)
     Ch, Dx = expected_terms(x[rows], D, C[rows], 1, H)
-    check_y(bits_of(out)[rows], ref_y, ref_states, Ch, Dx, 128)
-    mask = np.ones(2432, bool)
+    check_y(bits_of(out)[rows], ref_y, ref_states, Ch, Dx, N)
+    mask = np.ones(slots, bool)
     mask[idx] = False
     assert np.array_equal(got[mask], pool[mask])

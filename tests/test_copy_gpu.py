@@ -124,3 +124,31 @@ def test_copy_many_requests_many_tensors(op):
     perm = np.random.default_rng(4).permutation(96)
     skipped = _run_and_compare(op, specs, perm[:40].tolist(), perm[40:80].tolist(), seed=4)
     assert skipped == 0
+
+
+def test_copy_pages_layout_at_bench_size(op):
+    """The bench's workload on the table's launch shape for calls above 1 GiB: 48 tensors (24
+    fp32 blocks of 2 MiB, 24 bf16 blocks of 80 KiB per request, as on the vLLM page), 32
+    requests (3.3 GB per call), disjoint source and destination sets.  Checked on the device:
+    every destination block equals its source block byte for byte, every other block is
+    unchanged (compared against a copy taken before the call)."""
+    reqs = 32
+    blocks = 2 * reqs + 4
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    tensors = []
+    for shape, dtype in [((32, 128, 128), torch.float32)] * 24 + [((10240, 4), torch.bfloat16)] * 24:
+        t = torch.empty((blocks,) + shape, dtype=dtype, device="cuda")
+        t.uniform_(-1, 1, generator=gen)
+        tensors.append(t)
+    perm = torch.from_numpy(np.random.default_rng(11).permutation(blocks).astype(np.int32))
+    src, dst = perm[:reqs].cuda(), perm[reqs:2 * reqs].cuda()
+    rest = perm[2 * reqs:].cuda()
+    before_src = [t[src].clone() for t in tensors[:1]]   # spot copy of one tensor's sources
+    before_rest = [t[rest].clone() for t in tensors]
+    op.copy_blocks(tensors, src, dst)
+    torch.cuda.synchronize()
+    assert op.get_error() == (0, -1)
+    for t, r in zip(tensors, before_rest):
+        assert torch.equal(t[dst].view(torch.uint8), t[src].view(torch.uint8))
+        assert torch.equal(t[rest].view(torch.uint8), r.view(torch.uint8))
+    assert torch.equal(tensors[0][src].view(torch.uint8), before_src[0].view(torch.uint8))
