@@ -32,24 +32,26 @@ struct TokenParams {
     int bc_vec;  // B and C rows can be read as whole column pairs / quads (aligned vectors)
 };
 
-// update_lane (ssu_device.cuh) with the state update in packed fp32x2 instructions (two IEEE round-to-nearest
-// multiplies and two fused multiply-adds per pair of columns): the same values bit for bit,
-// with half the instructions for the update.  The readout chain stays scalar, in the same
-// order.  Used where instruction issue, not memory, bounds the kernel (the multi-token loop).
+// update_lane (ssu_device.cuh) on one lane's NC columns held as fp32 pairs (column 2i in .x,
+// 2i+1 in .y), the state update in packed fp32x2 instructions: two IEEE round-to-nearest
+// multiplies and two fused multiply-adds per pair, so the same values bit for bit, with half
+// the instructions.  The readout chain stays scalar, over the columns in the same order.
+// Holding the state and B/C as pairs for the whole token loop saves the moves that form
+// pairs out of scalar registers (measured 1-2 % faster at T >= 3).
 template <int NC>
-__device__ __forceinline__ float update_lane_packed(float (&v)[NC], float dA, float k,
-                                                    const float (&bb)[NC], const float (&cc)[NC]) {
-    const float2 dA2 = make_float2(dA, dA), k2 = make_float2(k, k);
+__device__ __forceinline__ float update_pairs(float2 (&w)[NC / 2], float2 dA2, float k,
+                                              const float2 (&b2)[NC / 2],
+                                              const float2 (&c2)[NC / 2]) {
+    const float2 k2 = make_float2(k, k);
 #pragma unroll
-    for (int j = 0; j < NC; j += 2) {
-        const float2 kb = __fmul2_rn(k2, make_float2(bb[j], bb[j + 1]));
-        const float2 r = __ffma2_rn(make_float2(v[j], v[j + 1]), dA2, kb);
-        v[j] = r.x;
-        v[j + 1] = r.y;
+    for (int i = 0; i < NC / 2; ++i) w[i] = __ffma2_rn(w[i], dA2, __fmul2_rn(k2, b2[i]));
+    float part = w[0].x * c2[0].x;
+    part = fmaf(w[0].y, c2[0].y, part);
+#pragma unroll
+    for (int i = 1; i < NC / 2; ++i) {
+        part = fmaf(w[i].x, c2[i].x, part);
+        part = fmaf(w[i].y, c2[i].y, part);
     }
-    float part = v[0] * cc[0];
-#pragma unroll
-    for (int j = 1; j < NC; ++j) part = fmaf(v[j], cc[j], part);
     return part;
 }
 
@@ -76,14 +78,12 @@ __device__ __forceinline__ float widen_bf16(unsigned short u) {
     return __uint_as_float(static_cast<unsigned>(u) << 16);  // exact: bf16 is fp32's top half
 }
 
-// Column j of a pair word array, widened to fp32.
+// Pair words widened to fp32 pairs.
 template <int NC>
-__device__ __forceinline__ void widen_pairs(const unsigned (&w)[NC / 2], float (&o)[NC]) {
+__device__ __forceinline__ void widen_pairs(const unsigned (&w)[NC / 2], float2 (&o)[NC / 2]) {
 #pragma unroll
-    for (int i = 0; i < NC / 2; ++i) {
-        o[2 * i] = __uint_as_float(w[i] << 16);
-        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < NC / 2; ++i)
+        o[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
 
 // The lane's NC columns starting at `p` (its first column) as pair words.  VEC: one 4- or
@@ -174,17 +174,24 @@ __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW]
     xn += PD * q.x_t;
     float lane_dtv, lane_dA;
     token_scalars(q, b, h, bias, Ah, 0, lane, lane_dtv, lane_dA);
+    float2 w[RPW][NC / 2];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int i = 0; i < NC / 2; ++i) w[r][i] = make_float2(v[r][2 * i], v[r][2 * i + 1]);
     for (int t0 = 0; t0 < q.tokens; t0 += PD) {
 #pragma unroll
         for (int k = 0; k < PD; ++k) {
             const int t = t0 + k;
             if (t >= q.tokens) break;
-            if (t > 0 && (t & 31) == 0) token_scalars(q, b, h, bias, Ah, t, lane, lane_dtv, lane_dA);
+            if (t > 0 && (t & 31) == 0)
+                token_scalars(q, b, h, bias, Ah, t, lane, lane_dtv, lane_dA);
             const float dtv = __shfl_sync(0xffffffffu, lane_dtv, t & 31);
             const float dA = __shfl_sync(0xffffffffu, lane_dA, t & 31);
-            float bb[NC], cc[NC];
-            widen_pairs<NC>(ring[k].b, bb);
-            widen_pairs<NC>(ring[k].c, cc);
+            float2 b2[NC / 2], c2[NC / 2];
+            widen_pairs<NC>(ring[k].b, b2);
+            widen_pairs<NC>(ring[k].c, c2);
+            const float2 dA2 = make_float2(dA, dA);
             const float xl = widen_bf16(ring[k].x);
             if (t + PD < q.tokens) load_token<NC, VEC>(Bn, Cn, xn, x_live, ring[k]);
             Bn += q.B_t;
@@ -194,14 +201,20 @@ __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW]
             float part[RPW];
 #pragma unroll
             for (int r = 0; r < RPW; ++r)
-                part[r] = update_lane_packed<NC>(v[r], dA, __shfl_sync(0xffffffffu, kl, r), bb,
-                                                 cc);
+                part[r] = update_pairs<NC>(w[r], dA2, __shfl_sync(0xffffffffu, kl, r), b2, c2);
             if (q.inter) {
                 ST *irow = static_cast<ST *>(q.inter) + b * q.in_b + t * q.in_t + h * q.in_h +
                            row0 * q.in_p + lo;
 #pragma unroll
-                for (int r = 0; r < RPW; ++r)
-                    if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, v[r]);
+                for (int r = 0; r < RPW; ++r) {
+                    float tmp[NC];
+#pragma unroll
+                    for (int i = 0; i < NC / 2; ++i) {
+                        tmp[2 * i] = w[r][i].x;
+                        tmp[2 * i + 1] = w[r][i].y;
+                    }
+                    if (row0 + r < p.headdim) store_cols<NC, ST>(irow + r * q.in_p, tmp);
+                }
             }
             const float total = reduce_rows<RPW>(part, lane);
             const int rl = row_of_lane<RPW>(lane);
@@ -211,6 +224,10 @@ __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW]
                     __float2bfloat16_rn(fmaf(Dh, xr, total));
         }
     }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int i = 0; i < NC / 2; ++i) v[r][2 * i] = w[r][i].x, v[r][2 * i + 1] = w[r][i].y;
 }
 
 // 16 rows per warp hold 64 state values per lane: those CTAs are limited to 4 warps so the
