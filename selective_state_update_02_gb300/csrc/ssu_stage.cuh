@@ -46,6 +46,14 @@ __device__ __forceinline__ void move_vec(const char *s, char *d) {
     *reinterpret_cast<V *>(d) = *reinterpret_cast<const V *>(s);
 }
 
+// Byte offsets, in the source and in the destination, of vector `local` of job J.
+__host__ __device__ __forceinline__ void stage_offsets(const StageJob &J, long long local,
+                                                       long long &src, long long &dst) {
+    const long long r = local / J.cpr, k = local - r * J.cpr;
+    src = (r / J.inner) * J.s_outer + (r % J.inner) * J.s_inner + k * J.vec;
+    dst = r * J.row_bytes + k * J.vec;
+}
+
 // One vector per thread and grid-stride iteration.  Waits for the previous grid in the stream
 // before the first access (a programmatic dependent launch may start it early) and lets the
 // update kernel's CTAs launch once its stores are issued; the update kernel in turn waits for
@@ -58,10 +66,10 @@ __global__ void __launch_bounds__(kStageThreads) ssu_stage_kernel(const StagePar
         int j = 0;
         while (j + 1 < q.njobs && c >= q.job[j + 1].chunk0) ++j;
         const StageJob &J = q.job[j];
-        const long long local = c - J.chunk0;
-        const long long r = local / J.cpr, k = local - r * J.cpr;
-        const char *s = J.src + (r / J.inner) * J.s_outer + (r % J.inner) * J.s_inner + k * J.vec;
-        char *d = J.dst + r * J.row_bytes + k * J.vec;
+        long long so, dof;
+        stage_offsets(J, c - J.chunk0, so, dof);
+        const char *s = J.src + so;
+        char *d = J.dst + dof;
         switch (J.vec) {
             case 16: move_vec<uint4>(s, d); break;
             case 8: move_vec<uint2>(s, d); break;
