@@ -793,7 +793,7 @@ def run_copy(args) -> None:
     handle = ssu.ssu_create(0)
     peaks = load_peaks()
     shapes = [None]
-    reqs_list = COPY_REQS
+    reqs_list = tuple(args.copy_reqs)
     if args.sweep:
         reqs_list = (8, 32, 128)
         shapes = ([(ssu.SSU_COPY_VEC, c, v, t) for c in (16, 32, 64) for v in (4, 8, 16)
@@ -1003,6 +1003,8 @@ def main() -> None:
     ap.add_argument("--sweep", action="store_true", help="launch-shape sweep instead")
     ap.add_argument("--calibrate", action="store_true",
                     help="library copy / in-place rates at the call sizes instead")
+    ap.add_argument("--copy-reqs", type=int, nargs="+", default=list(COPY_REQS),
+                    help="request counts timed by --copy")
     ap.add_argument("--tokens-list", type=int, nargs="+", default=[1, 2, 3, 4],
                     help="token counts timed by --tokens")
     ap.add_argument("--e2e-only", action="store_true",
