@@ -257,3 +257,30 @@ def test_rejections_before_any_launch(handle):
     assert e.value.status == ssu.SSU_ERR_MISALIGNED
     torch.cuda.synchronize()
     assert torch.equal(pool0, dev["state_pool"])          # nothing was launched
+
+
+@pytest.mark.parametrize("i64", [False, True])
+def test_strided_index_and_dt_views(handle, i64):
+    """Indices every other element of a wider pinned array, dt a [bs, H] view with head
+    stride 2: the staging jobs gather them; the step matches ssu_update on dense copies."""
+    bs, H = 12, 8
+    pr = wl.make_problem(bs, H, pool_size=20, seed=61)
+    ref = to_device(pr, "cuda", torch.int64 if i64 else torch.int32)
+    dev = to_device(pr, "cuda", torch.int64 if i64 else torch.int32)
+    hop = host_operands(pr, packed=True, i64=i64)
+    wide_idx = torch.zeros(2 * bs, dtype=hop["state_batch_indices"].dtype).pin_memory()
+    wide_idx[::2] = hop["state_batch_indices"]
+    wide_idx[1::2] = -7                       # never read
+    hop["state_batch_indices"] = wide_idx[::2]
+    wide_dt = torch.zeros(bs, 2 * H, dtype=torch.bfloat16).pin_memory()
+    wide_dt[:, ::2] = torch.from_numpy(pr.dt.view(np.int16)).view(torch.bfloat16)
+    hop["dt"] = wide_dt[:, ::2]
+    assert hop["state_batch_indices"].stride(0) == 2 and hop["dt"].stride(1) == 2
+    ws = workspace_for(dev, hop)
+    ssu.ssu_update(handle, **ref)
+    ssu.ssu_update_from_host(handle, dev["state_pool"], hop["state_batch_indices"], hop["x"],
+                             hop["dt"], dev["dt_bias"], dev["A"], hop["B"], hop["C"], dev["D"],
+                             hop["out"], ws)
+    torch.cuda.synchronize()
+    assert_same(ref, dev, hop)
+    assert ssu.ssu_get_error(handle) == (0, -1)
