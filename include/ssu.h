@@ -278,7 +278,8 @@ typedef struct {
  * Within a call the running state stays in fp32; a bf16 state is rounded only when written.
  * Same error behaviour as ssu_update; enqueued on `stream`; allocates and synchronises
  * nothing.  B and C are read as whole 4- or 8-byte column groups when their base and strides
- * allow it, element by element otherwise (same results either way).
+ * allow it, element by element otherwise (same results either way).  T = 1 without an
+ * intermediate buffer runs as ssu_update.
  */
 ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                                const void *state_batch_indices, const uint16_t *x,

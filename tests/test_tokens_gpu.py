@@ -207,3 +207,19 @@ def test_long_token_runs_cross_the_per_warp_scalar_batches(op):
     pr, x, dt, B, C = _tokens_problem(3, 40, H=4, seed=21)
     got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C)
     _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter)
+
+
+def test_one_token_with_intermediate_runs_the_token_kernel_bitwise(op):
+    """T = 1 with an intermediate buffer stays on the multi-token kernel (without one the call
+    runs as ssu_update): same bits as ssu_update, and the intermediate is the new state."""
+    pr, x, dt, B, C = _tokens_problem(12, 1, seed=2)
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, with_inter=True)
+    ref = to_device(pr, "cuda")
+    ref["x"], ref["dt"] = bf16_tensor(x[:, 0], "cuda"), bf16_tensor(dt[:, 0], "cuda")
+    ref["B"], ref["C"] = bf16_tensor(B[:, 0], "cuda"), bf16_tensor(C[:, 0], "cuda")
+    op(ref["state_pool"], ref["state_batch_indices"], ref["x"], ref["dt"], ref["dt_bias"],
+       ref["A"], ref["B"], ref["C"], ref["D"], ref["out"])
+    torch.cuda.synchronize()
+    assert np.array_equal(got_pool, ref["state_pool"].cpu().numpy())
+    assert np.array_equal(got_out[:, 0], bits_of(ref["out"]))
+    assert np.array_equal(got_inter[:, 0], got_pool[pr.idx])
