@@ -9,6 +9,46 @@
 
 namespace {
 
+// The lane's NC columns of B (or C) widened to fp32, read as whole 4- or 8-byte column groups.
+// Only for a warp whose first column address is aligned to that width (every lane then is).
+template <int NC>
+__device__ __forceinline__ void load_bc_vec(const __nv_bfloat16 *p, float (&o)[NC]) {
+    unsigned w[NC / 2];
+    if constexpr (NC == 2) {
+        w[0] = *reinterpret_cast<const unsigned *>(p);
+    } else {
+#pragma unroll
+        for (int g = 0; g < NC / 4; ++g) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(p + g * 128);
+            w[2 * g] = u.x;
+            w[2 * g + 1] = u.y;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NC / 2; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// Two ways of forming the per-row inputs, chosen per instantiation from a same-box A/B at batch
+// 128 (and 8 / 512 for fp32 at dstate 128), since the compiler's schedules differ:
+//  * kShuffleK: lane r < RPW loads x of row r and forms dt * x there; the other lanes get the
+//    product by a shuffle (instead of every lane loading every row's x and multiplying).  On
+//    for a bf16 state (dstate 128: 14.88 -> 13.78 us; 64: 11.91 -> 10.72) and for fp32 with 8
+//    rows per warp at dstate 128; off for fp32 at dstate 64 (13.26 -> 13.70) and with 2 rows
+//    per warp (batch 8: 3.56 -> 3.91).
+//  * kVectorBC: B and C read as 4- or 8-byte column groups when aligned.  On at dstate 256
+//    (bf16 26.51 -> 24.63; fp32 41.52 -> 41.14) and for fp32 with 8 rows per warp at dstate
+//    128 (both on: 22.99 -> 22.76 at batch 128, 81.03 -> 80.56 at 512); off at dstate 64
+//    (fp32 13.26 -> 14.61).
+// Every combination gives the same values bit for bit.
+template <int RPW, int NC, typename ST>
+struct VecForm {
+    static constexpr bool kShuffleK = sizeof(ST) == 2 || (NC == 4 && RPW >= 8);
+    static constexpr bool kVectorBC = NC == 8 || (NC == 4 && sizeof(ST) == 4 && RPW >= 8);
+};
+
 // Grid: x = slab of rows, y = head, z = request (requests beyond gridDim.z loop), so the
 // slot lookup at the head of the dependency chain needs no index arithmetic.
 template <int RPW, int NC, typename ST, bool kIdx64>
@@ -50,24 +90,48 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         const float Dh = p.D[h * p.D_h];
         const int g = h / p.heads_per_group;
         float bb[NC], cc[NC];
-        load_bc<NC>(p.B + b * p.B_b + g * p.B_g + lane_offset<NC>(lane), bb);
-        load_bc<NC>(p.C + b * p.C_b + g * p.C_g + lane_offset<NC>(lane), cc);
-        const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
-
-        float part[RPW];
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const bool live = row0 + r < p.headdim;
-            const float xr = live ? __bfloat162float(xp[r]) : 0.f;
-            part[r] = update_lane<NC>(v[r], dA, dtv * xr, bb, cc);
-            if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
+        const __nv_bfloat16 *Bw = p.B + b * p.B_b + g * p.B_g, *Cw = p.C + b * p.C_b + g * p.C_g;
+        if (VecForm<RPW, NC, ST>::kVectorBC &&
+            ((reinterpret_cast<unsigned long long>(Bw) | reinterpret_cast<unsigned long long>(Cw)) &
+             (NC == 2 ? 3u : 7u)) == 0) {
+            load_bc_vec<NC>(Bw + lane_offset<NC>(lane), bb);
+            load_bc_vec<NC>(Cw + lane_offset<NC>(lane), cc);
+        } else {
+            load_bc<NC>(Bw + lane_offset<NC>(lane), bb);
+            load_bc<NC>(Cw + lane_offset<NC>(lane), cc);
         }
-        const float total = reduce_rows<RPW>(part, lane);
-        const int rl = row_of_lane<RPW>(lane);
-        if (writes_row<RPW>(lane) && row0 + rl < p.headdim) {
-            const float xr = __bfloat162float(xp[rl]);
-            p.out[b * p.out_b + h * p.out_h + row0 + rl] =
-                __float2bfloat16_rn(fmaf(Dh, xr, total));
+        const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
+        float part[RPW];
+        if constexpr (VecForm<RPW, NC, ST>::kShuffleK) {
+            const bool x_live = lane < RPW && row0 + lane < p.headdim;
+            const float xl = x_live ? __bfloat162float(xp[lane]) : 0.f;
+            const float kl = dtv * xl;  // lane r < RPW: dt * x of row r
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                part[r] = update_lane<NC>(v[r], dA, __shfl_sync(0xffffffffu, kl, r), bb, cc);
+                if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
+            }
+            const float total = reduce_rows<RPW>(part, lane);
+            const int rl = row_of_lane<RPW>(lane);
+            const float xr = __shfl_sync(0xffffffffu, xl, rl);
+            if (writes_row<RPW>(lane) && row0 + rl < p.headdim)
+                p.out[b * p.out_b + h * p.out_h + row0 + rl] =
+                    __float2bfloat16_rn(fmaf(Dh, xr, total));
+        } else {
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const bool live = row0 + r < p.headdim;
+                const float xr = live ? __bfloat162float(xp[r]) : 0.f;
+                part[r] = update_lane<NC>(v[r], dA, dtv * xr, bb, cc);
+                if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
+            }
+            const float total = reduce_rows<RPW>(part, lane);
+            const int rl = row_of_lane<RPW>(lane);
+            if (writes_row<RPW>(lane) && row0 + rl < p.headdim) {
+                const float xr = __bfloat162float(xp[rl]);
+                p.out[b * p.out_b + h * p.out_h + row0 + rl] =
+                    __float2bfloat16_rn(fmaf(Dh, xr, total));
+            }
         }
     }
     pdl_trigger();  // this CTA's stores are issued: a dependent launch may start its CTAs
