@@ -48,6 +48,8 @@ PAGE_US = {8: 4.02, 128: 24.1, 512: 85.7}   # sglang PR #41223 Speedup Result, B
 CSRC = ROOT / "selective_state_update_02_gb300" / "csrc"
 KERNEL_SOURCES = [CSRC / "ssu_vec.cuh", CSRC / "ssu_device.cuh"]     # VEC kernel
 BULK_SOURCES = [CSRC / "ssu_bulk.cuh", CSRC / "ssu_device.cuh"]      # BULK kernel
+TOKENS_SOURCES = [CSRC / "ssu_tokens.cuh", CSRC / "ssu_device.cuh"]  # multi-token kernel
+COPY_SOURCES = [CSRC / "ssu_copy.cu"]                                # block-copy kernels
 
 
 # ---- arithmetic of the measurement (host logic, tested on CPU) ---------------------------
@@ -96,13 +98,14 @@ def source_digest(files=None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_tag: str, bulk: bool = False) -> int | None:
+def recorded_traffic(workload_tag: str, bulk: bool = False, sources=None) -> int | None:
     """DRAM bytes per launch from a committed ncu summary, if it was taken on this source.
 
     The summaries under profiles/ carry a line
-    ``traffic_per_launch_bytes: <int> source: <digest> workload: <tag>``.
+    ``traffic_per_launch_bytes: <int> source: <digest> workload: <tag>``.  The digest covers
+    ``sources`` (default: the VEC kernel's, or the BULK kernel's with ``bulk``).
     """
-    digest = source_digest(BULK_SOURCES if bulk else KERNEL_SOURCES)
+    digest = source_digest(sources or (BULK_SOURCES if bulk else KERNEL_SOURCES))
     for f in sorted((ROOT / "profiles").glob("*.md")):
         for m in re.finditer(r"traffic_per_launch_bytes:\s*(\d+)\s+source:\s*([0-9a-f]+)\s+"
                              r"workload:\s*(\S+)", f.read_text()):
@@ -459,17 +462,17 @@ def time_e2e(wl_, handle, steps: int, dev) -> dict:
 class OracleCall:
     """One decode step of the batch run by the double-precision oracle on the host cores."""
 
-    def __init__(self, bs: int, H: int, seed: int):
+    def __init__(self, bs: int, H: int, seed: int, N: int = DSTATE):
         import oracle
         import workloads as wl
         oracle.build()
         self.oracle = oracle
         rng = np.random.default_rng(seed)
         # the call's own slots: a pool of bs slots addressed by a random permutation
-        self.pool0 = wl.state_pool(rng, bs, H).astype(np.float64)
+        self.pool0 = wl.state_pool(rng, bs, H, N=N).astype(np.float64)
         self.idx = rng.permutation(bs).astype(np.int64)
         self.dt_bias, self.A, self.D = wl.head_params(rng, H)
-        self.x, self.dt, self.B, self.C = wl.request_inputs(rng, bs, H)
+        self.x, self.dt, self.B, self.C = wl.request_inputs(rng, bs, H, N=N)
         self.bs = bs
         self.threads = os.cpu_count() or 1
 
@@ -484,8 +487,8 @@ class OracleCall:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(bs: int, H: int, budget_s: float = 12.0) -> dict:
-    oc = OracleCall(bs, H, seed=7)
+def cpu_baseline(bs: int, H: int, budget_s: float = 12.0, N: int = DSTATE) -> dict:
+    oc = OracleCall(bs, H, seed=7, N=N)
     oc.run()
     times = []
     t_start = time.perf_counter()
@@ -498,11 +501,66 @@ def cpu_baseline(bs: int, H: int, budget_s: float = 12.0) -> dict:
     single = [oc.run(quarter) * (bs / quarter) for _ in range(3)]
     oc.threads = threads
     return {"value": round(med * 1e6, 1), "unit": UNIT, "cores": oc.threads, "kind": "oracle",
-            "sample": f"{len(times)} full calls (batch {bs}, {H} heads, headdim 64, dstate 128) "
+            "sample": f"{len(times)} full calls (batch {bs}, {H} heads, headdim 64, dstate {N}) "
                       f"of the fp64 C oracle split over {oc.threads} host threads; median",
             "single_thread_value": round(statistics.median(single) * 1e6, 1),
             "single_thread_sample": f"3 calls over {quarter} of the {bs} requests on one "
                                     f"thread, scaled to the full batch; median"}
+
+
+def cpu_baseline_tokens(bs: int, H: int, T: int, budget_s: float = 6.0) -> dict:
+    """The oracle's multi-token step (the single step applied T times, intermediate states
+    kept) on a bounded sample of the batch, scaled to the full call."""
+    import oracle
+    import workloads as wl
+    oracle.build()
+    rng = np.random.default_rng(11)
+    pool = wl.state_pool(rng, bs, H)
+    idx = rng.permutation(bs).astype(np.int64)
+    dt_bias, A, D = wl.head_params(rng, H)
+    per_tok = [wl.request_inputs(rng, bs, H) for _ in range(T)]
+    x, dt, B, C = (np.stack([pt[i] for pt in per_tok], axis=1) for i in range(4))
+    req = max(1, bs // 16)
+    oracle.ssu_tokens(pool[:0], idx[:0], x[:0], dt[:0], dt_bias, A, B[:0], C[:0], D)
+    times = []
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s and len(times) < 20:
+        sub = np.ascontiguousarray(pool[:req])
+        t0 = time.perf_counter()
+        oracle.ssu_tokens(sub, np.arange(req), x[:req], dt[:req], dt_bias, A, B[:req], C[:req],
+                          D)
+        times.append((time.perf_counter() - t0) * (bs / req))
+    return {"value": round(statistics.median(times) * 1e6, 1), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{len(times)} runs of the oracle's {T}-token step (fp64 C single step "
+                      f"applied {T} times, intermediate states kept) over {req} of the {bs} "
+                      f"requests ({H} heads, headdim 64, dstate 128) on one thread, scaled "
+                      f"to the full batch; median"}
+
+
+def cpu_baseline_copy(reqs: int, budget_s: float = 6.0) -> dict:
+    """The oracle's block copy (plain numpy assignment) of the page's per-request blocks, on a
+    bounded sample of the requests, scaled to the full call."""
+    import oracle
+    rng = np.random.default_rng(13)
+    blocks = 4
+    tensors = ([rng.standard_normal((blocks,) + COPY_TEMPORAL, dtype=np.float32)
+                for _ in range(COPY_LAYERS)] +
+               [rng.integers(0, 2 ** 16, (blocks,) + COPY_CONV, dtype=np.uint16)
+                for _ in range(COPY_LAYERS)])
+    src, dst = np.array([0, 1]), np.array([2, 3])
+    times = []
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s and len(times) < 20:
+        t0 = time.perf_counter()
+        oracle.copy_blocks(tensors, src, dst)
+        times.append((time.perf_counter() - t0) * reqs / len(src))
+    return {"value": round(statistics.median(times) * 1e6, 1), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{len(times)} runs of the oracle's copy (numpy; it copies each whole "
+                      f"tensor before assigning blocks) over {len(src)} requests of the page's "
+                      f"{2 * COPY_LAYERS} tensors with {blocks} blocks each, on one thread, "
+                      f"scaled to {reqs} requests; median"}
 
 
 # ---- main ---------------------------------------------------------------------------------
@@ -657,7 +715,7 @@ def run_ours(args) -> None:
     if not args.skip_e2e:
         line["e2e"] = time_e2e(main, handle, min(args.steps, args.e2e_steps), dev)
     if rank == 0 and world == 1 and not args.skip_cpu:
-        line["cpu_baseline"] = cpu_baseline(bs, NHEADS)
+        line["cpu_baseline"] = cpu_baseline(bs, NHEADS, N=N)
     ssu.ssu_destroy(handle)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -800,6 +858,7 @@ def run_copy(args) -> None:
                    for t in (128, 256)] +
                   [(ssu.SSU_COPY_BULK, c, st, 0) for c in (16, 32, 64) for st in (3, 4, 6)
                    if 128 + st * c * 1024 <= 220 * 1024])
+    cpu_copy = None
     for reqs in reqs_list:
         w = CopyWorkload(reqs, dev, l2)
         moved = 2 * reqs * copy_bytes_per_request()
@@ -836,6 +895,20 @@ def run_copy(args) -> None:
                    "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4),
                    "pages_gb200_gbs": PAGE_COPY_GBS.get(reqs), "calls": n, "sets": w.n_sets,
                    "launch": list(shape) if shape else "table"}
+            if shape is None:
+                rec["roofline"] = {
+                    "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                    "traffic": recorded_traffic(f"copy{reqs}", sources=COPY_SOURCES),
+                    "algorithmic_bytes_per_launch": moved, "peak_source": peaks["source"],
+                    "kernel": "copy_vec_kernel"}
+                if not args.skip_cpu:
+                    if cpu_copy is None:
+                        cpu_copy = cpu_baseline_copy(1)
+                    rec["cpu_baseline"] = cpu_copy | {
+                        "value": round(cpu_copy["value"] * reqs, 1),
+                        "sample": cpu_copy["sample"].replace("scaled to 1 requests",
+                                                             f"scaled to {reqs} requests")}
             print(json.dumps(rec), flush=True)
             del g
         del w
@@ -889,6 +962,7 @@ def run_tokens(args) -> None:
     if args.sweep:
         shapes = [(r, w) for r in (4, 8, 16) for w in (1, 2, 4)]
         tokens_list = (2, 4)
+    cpu_by_t = {}
     for T in tokens_list:
         x = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(
             (w.n_sets, bs, T, H, HEADDIM), dtype=np.float32)).view(np.int16)).view(
@@ -918,12 +992,24 @@ def run_tokens(args) -> None:
                                w.n_sets, calls=n)
             moved = bytes_per_call_tokens(bs, T, with_inter)
             gbs = moved / (us * 1e-6) / 1e9
-            print(json.dumps({"tokens": T, "batch": bs, "intermediate": with_inter,
-                              "launch": list(shape) if shape else "table",
-                              "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
-                              "gbs": round(gbs, 1),
-                              "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4)}),
-                  flush=True)
+            rec = {"tokens": T, "batch": bs, "intermediate": with_inter,
+                   "launch": list(shape) if shape else "table",
+                   "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
+                   "gbs": round(gbs, 1),
+                   "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4)}
+            if shape is None:
+                tag = f"tokens{T}-batch{bs}" + ("-inter" if with_inter else "")
+                rec["roofline"] = {
+                    "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                    "traffic": recorded_traffic(tag, sources=TOKENS_SOURCES),
+                    "algorithmic_bytes_per_launch": moved, "peak_source": peaks["source"],
+                    "kernel": "ssu_tokens_kernel"}
+                if not args.skip_cpu:
+                    if T not in cpu_by_t:
+                        cpu_by_t[T] = cpu_baseline_tokens(bs, H, T)
+                    rec["cpu_baseline"] = cpu_by_t[T]
+            print(json.dumps(rec), flush=True)
             del inter
         del x, bc, dt, out
         torch.cuda.empty_cache()
