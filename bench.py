@@ -49,7 +49,7 @@ CSRC = ROOT / "selective_state_update_02_gb300" / "csrc"
 KERNEL_SOURCES = [CSRC / "ssu_vec.cuh", CSRC / "ssu_device.cuh"]     # VEC kernel
 BULK_SOURCES = [CSRC / "ssu_bulk.cuh", CSRC / "ssu_device.cuh"]      # BULK kernel
 TOKENS_SOURCES = [CSRC / "ssu_tokens.cuh", CSRC / "ssu_device.cuh"]  # multi-token kernel
-COPY_SOURCES = [CSRC / "ssu_copy.cu"]                                # block-copy kernels
+COPY_SOURCES = [CSRC / "ssu_copy.cu", CSRC / "ssu_device.cuh"]       # block-copy kernels
 
 
 # ---- arithmetic of the measurement (host logic, tested on CPU) ---------------------------
