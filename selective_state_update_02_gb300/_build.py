@@ -11,8 +11,8 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 CSRC = PKG / "csrc"
-SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_tokens.cu", CSRC / "ssu_tokens_deep.cu",
-           CSRC / "ssu_copy.cu", CSRC / "ssu_host.cpp"]
+SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_tokens.cu", CSRC / "ssu_copy.cu",
+           CSRC / "ssu_host.cpp"]
 HEADERS = [ROOT / "include" / "ssu.h", CSRC / "ssu_device.cuh", CSRC / "ssu_host.h",
            CSRC / "ssu_vec.cuh", CSRC / "ssu_bulk.cuh", CSRC / "ssu_stage.cuh",
            CSRC / "ssu_tokens.cuh"]

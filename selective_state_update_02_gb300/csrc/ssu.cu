@@ -124,6 +124,7 @@ SsuParams make_params(void *state_pool, const void *idx, const uint16_t *x, cons
     p.nheads = static_cast<int>(s.nheads);
     p.headdim = static_cast<int>(s.headdim);
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
+    p.group_magic = group_magic(static_cast<unsigned>(p.heads_per_group));
     p.slabs = static_cast<int>(slabs);
     p.rows_per_cta = rows_per_tile;
     p.err = err;

@@ -36,6 +36,7 @@ struct SsuParams {
     long long pool_size;
     long long batch;
     int nheads, headdim, heads_per_group;
+    unsigned long long group_magic;  // group_magic(heads_per_group): see group_of
     int slabs;         // tiles per (request, head) unit
     int rows_per_cta;  // rows per tile
     unsigned *err;     // [0] skipped requests, [1] smallest skipped request, [2] timeouts
@@ -46,6 +47,19 @@ struct BulkShape {
     long long tiles;  // batch * nheads * slabs
     int stages;
 };
+
+// Group of head h, floor(h / d) for d = heads per group, without an integer division (the
+// division by a value known only at run time expands into a long instruction sequence).  With
+// m = floor(2^32 / d) + 1 = 2^32 / d + e, 0 < e <= 1:  h m / 2^32 = h / d + h e / 2^32, and
+// for h, d < 2^16 the second term is below 2^-16 < 1 / d, so it cannot carry h / d past the
+// next integer: floor(h m / 2^32) = floor(h / d).  Heads are limited to 65535.
+__host__ __device__ inline unsigned long long group_magic(unsigned d) {
+    return (1ull << 32) / d + 1;
+}
+
+__host__ __device__ __forceinline__ int group_of(int h, unsigned long long m) {
+    return static_cast<int>((static_cast<unsigned long long>(h) * m) >> 32);
+}
 
 __device__ __forceinline__ float softplus_f32(float z) {
     // log(1 + e^z); above 20 the correction is below fp32 resolution of z.

@@ -26,11 +26,6 @@ ssu_status_t validate_impl(const void *state_pool, const void *idx, const uint16
 // (called once per handle by ssu_create, on the handle's device).
 cudaError_t copy_prepare(int smem_optin);
 
-// Launches the multi-token kernel with a prefetch ring of 4 tokens (ssu_tokens_deep.cu).
-// `params` is the TokenParams block of ssu_tokens.cuh, `bytes` its size.
-cudaError_t tokens_launch_depth4(const void *params, size_t bytes, int nc, bool bf16, bool i64,
-                                 int rpw, int wpc, dim3 grid, bool pdl, cudaStream_t st);
-
 // Restores the caller's current device on scope exit.
 struct DeviceGuard {
     int prev = -1;

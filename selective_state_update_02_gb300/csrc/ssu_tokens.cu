@@ -1,5 +1,5 @@
 // Multi-token decode step: the C entry point ssu_update_tokens (validation, launch shape) and
-// the kernels with a prefetch ring of 2 tokens; the kernel itself is in ssu_tokens.cuh.
+// the kernels' instantiations; the kernel itself is in ssu_tokens.cuh.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -106,6 +106,7 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     p.nheads = static_cast<int>(s.nheads);
     p.headdim = static_cast<int>(s.headdim);
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
+    p.group_magic = group_magic(static_cast<unsigned>(p.heads_per_group));
     p.slabs = static_cast<int>(slabs);
     p.rows_per_cta = rows_per_tile;
     p.err = handle->err;
@@ -140,11 +141,8 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                     static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
     const int nc = static_cast<int>(s.dstate / 32);
     const bool bf16 = s.state_dtype == SSU_STATE_BF16, i64 = s.index_dtype == SSU_INDEX_I64;
-    const cudaError_t e =
-        token_prefetch(tokens, s.dstate) == 4
-            ? ssu_host::tokens_launch_depth4(&q, sizeof(q), nc, bf16, i64, rpw, wpc, grid,
-                                             handle->pdl, cs)
-            : launch_tokens_depth<2>(q, nc, bf16, i64, rpw, wpc, grid, handle->pdl, cs);
+    const cudaError_t e = launch_tokens_depth<kTokenPrefetch>(q, nc, bf16, i64, rpw, wpc, grid,
+                                                              handle->pdl, cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -1,6 +1,5 @@
-// Multi-token decode-step kernel for GB300 (sm_103a), shared by the translation units that
-// instantiate it (ssu_tokens.cu: prefetch ring of 2 tokens and the C entry point;
-// ssu_tokens_deep.cu: ring of 4).
+// Multi-token decode-step kernel for GB300 (sm_103a), instantiated by ssu_tokens.cu (which
+// also holds the C entry point).
 //
 // The step: T consecutive tokens of every request in one
 // call (the verification step of multi-token speculation, vLLM PR #48110, Test Plan).  Token t
@@ -66,13 +65,14 @@ struct TokenBits {
 };
 
 // Tokens whose inputs a warp keeps in flight (the kernels' PD): the loads of token t + PD are
-// issued as soon as token t's inputs have been widened.  Measured at batch 128, dstate 128: a
-// ring of 2 is best up to 2 tokens, a ring of 4 from 3 tokens on (T = 4: 30.4 us against 31.9;
-// T = 8: 45.3 against 47.3).  At dstate 256 a ring of 4 does not fit the registers (it spills)
-// and is slower, so that bucket keeps 2.
-inline int token_prefetch(long long tokens, long long dstate) {
-    return tokens >= 3 && dstate <= 128 ? 4 : 2;
-}
+// issued as soon as token t's inputs have been widened.  A ring of 2, with the 8-row kernels
+// up to dstate 128 held to 96 registers (tokens_max_regs below: 21 resident warps per SM
+// instead of 16 at 125 registers), measured faster than a ring of 4 without the cap at every
+// token count, batch 128 (fp32 dstate 128, T = 2 / 3 / 4 / 8: 24.11 / 26.87 / 29.39 / 41.74 ->
+// 23.99 / 26.01 / 28.70 / 40.26 us; fp32 dstate 64, T = 4: 22.07 -> 20.49; bf16 dstate 128,
+// T = 4: 30.41 -> 26.79).  A ring of 3 at 104 registers was slower (T = 4: 30.50), a ring of 4
+// spills under a cap of 112 or less, and a ring of 2 spills under 88.
+constexpr int kTokenPrefetch = 2;
 
 __device__ __forceinline__ float widen_bf16(unsigned short u) {
     return __uint_as_float(static_cast<unsigned>(u) << 16);  // exact: bf16 is fp32's top half
@@ -154,7 +154,7 @@ __device__ __forceinline__ void token_loop(const TokenParams &q, float (&v)[RPW]
     const float bias = p.dt_bias[h * p.bias_h];
     const float Ah = p.A[h * p.A_h];
     const float Dh = p.D[h * p.D_h];
-    const int g = h / p.heads_per_group;
+    const int g = group_of(h, p.group_magic);
     const int lo = lane_offset<NC>(lane);
     const unsigned short *Bn = reinterpret_cast<const unsigned short *>(p.B) + b * p.B_b +
                                g * p.B_g + lo;
@@ -237,8 +237,16 @@ constexpr int tokens_max_threads() {
     return RPW >= 16 ? 128 : 32 * kMaxWarpsPerCta;
 }
 
+// Registers per thread: what the largest CTA allows (tokens_max_threads), except for the 8-row
+// kernels up to dstate 128 (the table's shape), held to 96 so 21 warps fit on an SM; with a
+// ring of 2 they need no spill at that cap (see kTokenPrefetch).
+template <int RPW, int NC>
+constexpr int tokens_max_regs() {
+    return RPW == 8 && NC <= 4 ? 96 : (RPW >= 16 ? 255 : 65536 / tokens_max_threads<RPW>());
+}
+
 template <int RPW, int NC, typename ST, bool kIdx64, int PD>
-__global__ void __launch_bounds__(tokens_max_threads<RPW>())
+__global__ void __maxnreg__((tokens_max_regs<RPW, NC>()))
     ssu_tokens_kernel(const __grid_constant__ TokenParams q) {
     pdl_wait();
     const SsuParams &p = q.p;
@@ -314,8 +322,7 @@ cudaError_t launch_tokens_t(const TokenParams &q, int rpw, int wpc, dim3 grid, b
 }
 
 // Launches the multi-token kernel with a prefetch ring of PD tokens for dstate = 32 * nc, a
-// bf16 or fp32 state, int64 or int32 indices (rings deeper than 2 only up to dstate 128).
-// Each translation unit instantiates one PD.
+// bf16 or fp32 state, int64 or int32 indices.
 template <int PD>
 cudaError_t launch_tokens_depth(const TokenParams &q, int nc, bool bf16, bool i64, int rpw,
                                 int wpc, dim3 grid, bool pdl, cudaStream_t st) {
@@ -329,7 +336,7 @@ cudaError_t launch_tokens_depth(const TokenParams &q, int nc, bool bf16, bool i6
     }
     SSU_TOK_NC(2)
     SSU_TOK_NC(4)
-    if constexpr (PD <= 2) SSU_TOK_NC(8)
+    SSU_TOK_NC(8)
 #undef SSU_TOK_NC
 #undef SSU_TOK_T
     return cudaErrorInvalidValue;

@@ -42,11 +42,17 @@ __device__ __forceinline__ void load_bc_vec(const __nv_bfloat16 *p, float (&o)[N
 //    (bf16 26.51 -> 24.63; fp32 41.52 -> 41.14) and for fp32 with 8 rows per warp at dstate
 //    128 (both on: 22.99 -> 22.76 at batch 128, 81.03 -> 80.56 at 512); off at dstate 64
 //    (fp32 13.26 -> 14.61).
+//  * kGroupMagic: the head's group from group_of (a multiply and a shift) instead of an integer
+//    division.  On with 8 rows per warp where a lane's part of a row is one 16-byte vector
+//    (fp32 at dstate 128: 22.76 -> 22.65 at batch 128, 80.68 -> 80.53 at 512; bf16 at dstate
+//    256: 24.67 -> 24.55); off elsewhere (fp32 batch 8: 3.56 -> 3.95; bf16 dstate 128: 13.84
+//    -> 15.43; dstate 64 fp32 13.29 -> 13.74, bf16 10.74 -> 11.12; fp32 dstate 256 unchanged).
 // Every combination gives the same values bit for bit.
 template <int RPW, int NC, typename ST>
 struct VecForm {
     static constexpr bool kShuffleK = sizeof(ST) == 2 || (NC == 4 && RPW >= 8);
     static constexpr bool kVectorBC = NC == 8 || (NC == 4 && sizeof(ST) == 4 && RPW >= 8);
+    static constexpr bool kGroupMagic = RPW >= 8 && NC * sizeof(ST) == 16;
 };
 
 // Grid: x = slab of rows, y = head, z = request (requests beyond gridDim.z loop), so the
@@ -88,7 +94,8 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         const float dtv = softplus_f32(z);
         const float dA = expf(dtv * p.A[h * p.A_h]);
         const float Dh = p.D[h * p.D_h];
-        const int g = h / p.heads_per_group;
+        const int g = VecForm<RPW, NC, ST>::kGroupMagic ? group_of(h, p.group_magic)
+                                                        : h / p.heads_per_group;
         float bb[NC], cc[NC];
         const __nv_bfloat16 *Bw = p.B + b * p.B_b + g * p.B_g, *Cw = p.C + b * p.C_b + g * p.C_g;
         if (VecForm<RPW, NC, ST>::kVectorBC &&

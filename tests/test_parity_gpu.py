@@ -103,6 +103,22 @@ def test_every_launch_shape_is_bitwise_identical(op, P):
         op.set_launch(ssu.SSU_MODE_AUTO)
 
 
+@pytest.mark.parametrize("H,G", [(12, 3), (16, 4), (48, 16)])
+def test_every_vec_shape_with_groups(op, H, G):
+    # Several heads per group: each VEC shape (whichever way it forms a head's group index)
+    # reads its B and C rows from group h / (H / G), checked against the oracle at every shape.
+    pr = wl.make_problem(5, H, G=G, pool_size=11, seed=H + G)
+    try:
+        for shape in VEC_SHAPES:
+            t = to_device(pr, DEV)
+            op.set_launch(*shape)
+            _run(op, t)
+            _compare_all(pr, t, pr.pool)
+        assert op.get_error() == (0, -1)
+    finally:
+        op.set_launch(ssu.SSU_MODE_AUTO)
+
+
 @pytest.mark.parametrize("shape", [(ssu.SSU_MODE_BULK, 8, 4, 4), (ssu.SSU_MODE_BULK, 2, 1, 2),
                                    (ssu.SSU_MODE_BULK, 16, 8, 3)])
 @pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
