@@ -66,11 +66,11 @@ struct TokenBits {
 
 // Tokens whose inputs a warp keeps in flight (the kernels' PD): the loads of token t + PD are
 // issued as soon as token t's inputs have been widened.  A ring of 2, with the 8-row kernels
-// up to dstate 128 held to 96 registers (tokens_max_regs below: 21 resident warps per SM
-// instead of 16 at 125 registers), measured faster than a ring of 4 without the cap at every
-// token count, batch 128 (fp32 dstate 128, T = 2 / 3 / 4 / 8: 24.11 / 26.87 / 29.39 / 41.74 ->
-// 23.99 / 26.01 / 28.70 / 40.26 us; fp32 dstate 64, T = 4: 22.07 -> 20.49; bf16 dstate 128,
-// T = 4: 30.41 -> 26.79).  A ring of 3 at 104 registers was slower (T = 4: 30.50), a ring of 4
+// up to dstate 128 held to 96 registers (tokens_max_regs below: 20 resident warps per SM, 5
+// per sub-partition's register file, instead of 16 at 125 registers), measured faster than a
+// ring of 4 without the cap at every token count, batch 128 (fp32 dstate 128, T = 2 / 3 / 4 /
+// 8: 24.11 / 26.87 / 29.39 / 41.74 -> 23.99 / 26.01 / 28.70 / 40.26 us; fp32 dstate 64, T = 4:
+// 22.07 -> 20.49; bf16 dstate 128, T = 4: 30.41 -> 26.79).  A ring of 3 at 104 registers was slower (T = 4: 30.50), a ring of 4
 // spills under a cap of 112 or less, and a ring of 2 spills under 88.
 constexpr int kTokenPrefetch = 2;
 
@@ -238,7 +238,7 @@ constexpr int tokens_max_threads() {
 }
 
 // Registers per thread: what the largest CTA allows (tokens_max_threads), except for the 8-row
-// kernels up to dstate 128 (the table's shape), held to 96 so 21 warps fit on an SM; with a
+// kernels up to dstate 128 (the table's shape), held to 96 so 20 warps fit on an SM; with a
 // ring of 2 they need no spill at that cap (see kTokenPrefetch).
 template <int RPW, int NC>
 constexpr int tokens_max_regs() {
