@@ -635,8 +635,7 @@ def run_ours(args) -> None:
     handle = ssu.ssu_create(local)
     if args.launch:
         ssu.ssu_set_launch(handle, *[int(v) for v in args.launch.split(",")])
-    if args.pdl:
-        ssu.ssu_set_pdl(handle, True)
+    ssu.ssu_set_pdl(handle, not args.no_pdl)
     warmup = max(args.warmup, 3)
     bs = args.batch
     N, sdt = args.dstate, args.state_dtype
@@ -676,7 +675,7 @@ def run_ours(args) -> None:
         "config": config_for(bs, main.n_sets, N, sdt) | {
             "launch": {"mode": launch[0], "rows_per_warp": launch[1],
                        "warps_per_cta": launch[2], "stages": launch[3],
-                       "programmatic_dependent_launch": bool(args.pdl)}},
+                       "programmatic_dependent_launch": not args.no_pdl}},
         "achieved_tbps": round(achieved_gbs / 1000.0, 3),
         "pct_of_nominal_8tbps": round(100.0 * achieved_gbs / NOMINAL_HBM_GBS, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1),
@@ -1084,8 +1083,9 @@ def main() -> None:
                     help="multi-token step (T = 1..4) at --batch instead")
     ap.add_argument("--copy", action="store_true",
                     help="state-block copy throughput instead (with --sweep: its shapes)")
-    ap.add_argument("--pdl", action="store_true",
-                    help="launch as programmatic dependents (ssu_set_pdl); off by default")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch (ssu_set_pdl(h, 0)); "
+                         "it is on by default")
     ap.add_argument("--sweep", action="store_true", help="launch-shape sweep instead")
     ap.add_argument("--calibrate", action="store_true",
                     help="library copy / in-place rates at the call sizes instead")

@@ -377,7 +377,7 @@ def ssu_check_indices(state_batch_indices, pool_size: int) -> int:
 
 
 def ssu_set_pdl(handle: int, enable: bool = True) -> None:
-    """Opt in or out of programmatic dependent launch for this handle (off by default)."""
+    """Turn programmatic dependent launch on or off for this handle (on by default)."""
     _check(lib().ssu_set_pdl(handle, 1 if enable else 0), "ssu_set_pdl")
 
 

@@ -54,5 +54,5 @@ struct ssu_handle_s {
     ssu_launch_t override_launch{};
     bool has_copy_override = false;
     ssu_copy_launch_t copy_override{};
-    bool pdl = false;  // launch the VEC and multi-token kernels as programmatic dependents
+    bool pdl = true;  // launch the VEC and multi-token kernels as programmatic dependents
 };

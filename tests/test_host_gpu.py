@@ -148,7 +148,7 @@ def test_consecutive_steps_reuse_one_workspace(handle, pdl):
                                      hop["C"], dev["D"], hop["out"], ws)
         torch.cuda.synchronize()
     finally:
-        ssu.ssu_set_pdl(handle, False)
+        ssu.ssu_set_pdl(handle, True)  # the default
     for hop in steps:
         r = dict(ref)
         r.update({k: hop[k].cuda() for k in ("state_batch_indices", "x", "B", "C")})
