@@ -415,3 +415,32 @@ def test_pool_beyond_2_31_elements(op):
     assert not pool[mask].any()
     del pool
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("G", [3, 65535])
+def test_most_heads_with_groups(op, G):
+    # The largest head count the library accepts (65535), in 3 groups of 21845 heads or one
+    # head per group, on the table's 8-rows-per-warp launch (headdim 8): the head's group is
+    # h / (H / G) for every head, up to h = 65534.
+    H, P, bs = 65535, 8, 2
+    rng = np.random.default_rng(G)
+    pool = wl.state_pool(rng, bs + 1, H, P=P)                   # slot 1 stays untouched
+    idx = np.array([2, 0], dtype=np.int64)
+    dt_bias, A, D = wl.head_params(rng, H)
+    x, dt, B, C = wl.request_inputs(rng, bs, H, P=P, G=G)
+    t = dict(state_pool=torch.from_numpy(pool).to(DEV),
+             state_batch_indices=torch.from_numpy(idx).to(DEV).int(),
+             x=bf16_tensor(x, DEV), dt=bf16_tensor(dt, DEV),
+             dt_bias=torch.from_numpy(dt_bias).to(DEV), A=torch.from_numpy(A).to(DEV),
+             B=bf16_tensor(B, DEV), C=bf16_tensor(C, DEV), D=torch.from_numpy(D).to(DEV),
+             out=torch.zeros(bs, H, P, dtype=torch.bfloat16, device=DEV))
+    _run(op, t)
+    torch.cuda.synchronize()
+    got = t["state_pool"].cpu().numpy()
+    assert np.array_equal(got[1], pool[1])
+    ref_states, ref_y = oracle_on_requests(pool, idx, np.arange(bs), x, dt, dt_bias, A, B, C, D,
+                                           G)
+    check_state(got[idx], ref_states)
+    Ch, Dx = expected_terms(x, D, C, G, H)
+    check_y(bits_of(t["out"]), ref_y, ref_states, Ch, Dx, 128)
+    assert op.get_error() == (0, -1)
