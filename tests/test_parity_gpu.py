@@ -444,3 +444,21 @@ def test_most_heads_with_groups(op, G):
     Ch, Dx = expected_terms(x, D, C, G, H)
     check_y(bits_of(t["out"]), ref_y, ref_states, Ch, Dx, 128)
     assert op.get_error() == (0, -1)
+
+
+def test_degenerate_value_regimes(op):
+    # Heads 0-3: dt + dt_bias above 20, where softplus is z itself; heads 4-7: far below zero,
+    # so dt is ~1e-13 and dA rounds to 1 (the state carries over); heads 8-11: dt ~10 with
+    # A = -16, so dA underflows to 0 in fp32 (the state is replaced by dt x B); heads 12-15 as
+    # drawn.  Request 1 has x = 0 (pure decay, readout S'C), request 2 has C = 0 (readout D x).
+    pr = wl.make_problem(6, 16, pool_size=9, seed=41)
+    pr.dt_bias[0:4] = 25.0
+    pr.dt_bias[4:8] = -30.0
+    pr.dt_bias[8:12] = 10.0
+    pr.A[8:12] = -16.0
+    pr.x[1] = 0
+    pr.C[2] = 0
+    t = to_device(pr, DEV)
+    _run(op, t)
+    assert op.get_error() == (0, -1)
+    _compare_all(pr, t, pr.pool)

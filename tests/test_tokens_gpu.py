@@ -223,3 +223,21 @@ def test_one_token_with_intermediate_runs_the_token_kernel_bitwise(op):
     assert np.array_equal(got_pool, ref["state_pool"].cpu().numpy())
     assert np.array_equal(got_out[:, 0], bits_of(ref["out"]))
     assert np.array_equal(got_inter[:, 0], got_pool[pr.idx])
+
+
+@pytest.mark.parametrize("N", [128, 256])
+def test_most_tokens_per_call(op, N):
+    """The largest token count one call takes (SSU_MAX_TOKENS = 64): every token's readout and
+    intermediate state against the oracle; one more token is refused before any launch."""
+    pr = wl.make_problem(3, 4, 64, N, 1, pool_size=5, seed=31)
+    rng = np.random.default_rng(38)
+    steps = [wl.request_inputs(rng, 3, 4, 64, N, 1) for _ in range(64)]
+    x, dt, B, C = (np.stack([s[i] for s in steps], 1) for i in range(4))
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C)
+    _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter)
+    assert op.get_error() == (0, -1)
+    steps.append(wl.request_inputs(rng, 3, 4, 64, N, 1))
+    x, dt, B, C = (np.stack([s[i] for s in steps], 1) for i in range(4))
+    with pytest.raises(ssu.SsuError) as e:
+        _run(op, pr, x, dt, B, C, with_inter=False)
+    assert e.value.status == ssu.SSU_ERR_INVALID_ARG
