@@ -848,6 +848,7 @@ def run_copy(args) -> None:
     dev = torch.device("cuda", 0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     handle = ssu.ssu_create(0)
+    ssu.ssu_set_pdl(handle, not args.no_pdl)
     peaks = load_peaks()
     shapes = [None]
     reqs_list = tuple(args.copy_reqs)
@@ -893,7 +894,8 @@ def run_copy(args) -> None:
             rec = {"copy_reqs": reqs, "us_per_call": round(best, 3), "gbs": round(gbs, 1),
                    "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4),
                    "pages_gb200_gbs": PAGE_COPY_GBS.get(reqs), "calls": n, "sets": w.n_sets,
-                   "launch": list(shape) if shape else "table"}
+                   "launch": list(shape) if shape else "table",
+                   "programmatic_dependent_launch": not args.no_pdl}
             if shape is None:
                 rec["roofline"] = {
                     "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
@@ -952,6 +954,7 @@ def run_tokens(args) -> None:
     dev = torch.device("cuda", 0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     handle = ssu.ssu_create(0)
+    ssu.ssu_set_pdl(handle, not args.no_pdl)
     bs, H = args.batch, NHEADS
     w = Workload(bs, H, dev, seed=5, l2_bytes=l2)
     rng = np.random.default_rng(9)
@@ -993,6 +996,7 @@ def run_tokens(args) -> None:
             gbs = moved / (us * 1e-6) / 1e9
             rec = {"tokens": T, "batch": bs, "intermediate": with_inter,
                    "launch": list(shape) if shape else "table",
+                   "programmatic_dependent_launch": not args.no_pdl,
                    "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
                    "gbs": round(gbs, 1),
                    "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4)}

@@ -243,7 +243,8 @@ ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
  * each CTA releases its own dependents once its stores are issued.  This hides part of the
  * launch gap between back-to-back kernels (batch 8: 3.75 -> 3.38 us per call).  Work other
  * than a kernel (a copy, an event wait) still completes before the launch starts, as in any
- * stream.  BULK, copy and allocation-free launches never use it.
+ * stream.  The VEC block copy (ssu_copy_blocks) follows the same setting; BULK launches (of
+ * the decode step and of the copy) and the allocation-free entry point never use it.
  */
 ssu_status_t ssu_set_pdl(ssu_handle_t handle, int32_t enable);
 

@@ -90,8 +90,12 @@ __device__ __forceinline__ ChunkRef locate_chunk(const CopyParams &p, long long 
     return r;
 }
 
+// Launched as a programmatic dependent when the handle says so: nothing is read or written
+// before the previous kernel in the stream has completed (pdl_wait), and each CTA lets a
+// dependent launch start once its last stores are issued.
 template <int V>
 __global__ void __launch_bounds__(256) copy_vec_kernel(const __grid_constant__ CopyParams p) {
+    pdl_wait();
     const long long pass = static_cast<long long>(blockDim.x) * 16 * V;
     for (long long c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
         const ChunkRef r = locate_chunk(p, c);
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(256) copy_vec_kernel(const __grid_constant__ C
             }
         }
     }
+    pdl_trigger();
 }
 
 __device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, unsigned bytes) {
@@ -189,17 +194,31 @@ __global__ void __launch_bounds__(32) copy_bulk_kernel(const __grid_constant__ C
     }
 }
 
+template <int V>
+cudaError_t launch_copy_vec_one(const CopyParams &p, int threads, unsigned grid, bool pdl,
+                                cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, copy_vec_kernel<V>, p);
+}
+
 cudaError_t launch_copy_vec(const CopyParams &p, int vectors, int threads, unsigned grid,
-                            cudaStream_t st) {
+                            bool pdl, cudaStream_t st) {
     switch (vectors) {
-        case 1: copy_vec_kernel<1><<<grid, threads, 0, st>>>(p); break;
-        case 2: copy_vec_kernel<2><<<grid, threads, 0, st>>>(p); break;
-        case 4: copy_vec_kernel<4><<<grid, threads, 0, st>>>(p); break;
-        case 8: copy_vec_kernel<8><<<grid, threads, 0, st>>>(p); break;
-        case 16: copy_vec_kernel<16><<<grid, threads, 0, st>>>(p); break;
+        case 1: return launch_copy_vec_one<1>(p, threads, grid, pdl, st);
+        case 2: return launch_copy_vec_one<2>(p, threads, grid, pdl, st);
+        case 4: return launch_copy_vec_one<4>(p, threads, grid, pdl, st);
+        case 8: return launch_copy_vec_one<8>(p, threads, grid, pdl, st);
+        case 16: return launch_copy_vec_one<16>(p, threads, grid, pdl, st);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 using VecCopyKernel = void (*)(CopyParams);
@@ -339,7 +358,7 @@ ssu_status_t ssu_copy_blocks(ssu_handle_t handle, const ssu_block_tensor_t *tens
         if (e == cudaSuccess) {
             const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
             const unsigned grid = static_cast<unsigned>(chunks < slots ? chunks : slots);
-            e = launch_copy_vec(p, l.stages, l.threads, grid, cs);
+            e = launch_copy_vec(p, l.stages, l.threads, grid, handle->pdl, cs);
         }
     }
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "copy launch: %s", cudaGetErrorString(e));
