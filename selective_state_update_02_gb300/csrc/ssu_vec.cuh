@@ -47,13 +47,48 @@ __device__ __forceinline__ void load_bc_vec(const __nv_bfloat16 *p, float (&o)[N
 //    (fp32 at dstate 128: 22.76 -> 22.65 at batch 128, 80.68 -> 80.53 at 512; bf16 at dstate
 //    256: 24.67 -> 24.55); off elsewhere (fp32 batch 8: 3.56 -> 3.95; bf16 dstate 128: 13.84
 //    -> 15.43; dstate 64 fp32 13.29 -> 13.74, bf16 10.74 -> 11.12; fp32 dstate 256 unchanged).
+//  * kPacked: the state update in packed fp32x2 multiplies and fused multiply-adds (IEEE round
+//    to nearest per element, the same values).  On for a bf16 state (dstate 128 / 256 / 64:
+//    13.50 -> 13.42, 24.22 -> 24.07, 10.59 -> 10.47 us at batch 128) and for fp32 with 8 rows
+//    per warp at dstate 128 (22.34 -> 22.27 at batch 128, 80.17 -> 80.09 at 512); off for fp32
+//    at dstate 64 and 256 (13.00 -> 13.56, 40.94 -> 42.30: more registers, fewer warps).
 // Every combination gives the same values bit for bit.
 template <int RPW, int NC, typename ST>
 struct VecForm {
     static constexpr bool kShuffleK = sizeof(ST) == 2 || (NC == 4 && RPW >= 8);
     static constexpr bool kVectorBC = NC == 8 || (NC == 4 && sizeof(ST) == 4 && RPW >= 8);
     static constexpr bool kGroupMagic = RPW >= 8 && NC * sizeof(ST) == 16;
+    static constexpr bool kPacked = sizeof(ST) == 2 || (NC == 4 && RPW == 8);
 };
+
+// update_lane (ssu_device.cuh) with the state update in packed fp32x2 instructions; the
+// readout chain stays scalar, over the columns in the same order.
+template <int NC>
+__device__ __forceinline__ float update_lane_packed(float (&v)[NC], float dA, float k,
+                                                    const float (&bb)[NC],
+                                                    const float (&cc)[NC]) {
+    const float2 k2 = make_float2(k, k), dA2 = make_float2(dA, dA);
+#pragma unroll
+    for (int i = 0; i < NC / 2; ++i) {
+        const float2 w = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), dA2,
+                                    __fmul2_rn(k2, make_float2(bb[2 * i], bb[2 * i + 1])));
+        v[2 * i] = w.x;
+        v[2 * i + 1] = w.y;
+    }
+    float part = v[0] * cc[0];
+#pragma unroll
+    for (int j = 1; j < NC; ++j) part = fmaf(v[j], cc[j], part);
+    return part;
+}
+
+template <int RPW, int NC, typename ST>
+__device__ __forceinline__ float update_row(float (&v)[NC], float dA, float k,
+                                            const float (&bb)[NC], const float (&cc)[NC]) {
+    if constexpr (VecForm<RPW, NC, ST>::kPacked)
+        return update_lane_packed<NC>(v, dA, k, bb, cc);
+    else
+        return update_lane<NC>(v, dA, k, bb, cc);
+}
 
 // Grid: x = slab of rows, y = head, z = request (requests beyond gridDim.z loop), so the
 // slot lookup at the head of the dependency chain needs no index arithmetic.
@@ -115,7 +150,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
             const float kl = dtv * xl;  // lane r < RPW: dt * x of row r
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
-                part[r] = update_lane<NC>(v[r], dA, __shfl_sync(0xffffffffu, kl, r), bb, cc);
+                part[r] = update_row<RPW, NC, ST>(v[r], dA, __shfl_sync(0xffffffffu, kl, r), bb, cc);
                 if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
             }
             const float total = reduce_rows<RPW>(part, lane);
@@ -129,7 +164,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
             for (int r = 0; r < RPW; ++r) {
                 const bool live = row0 + r < p.headdim;
                 const float xr = live ? __bfloat162float(xp[r]) : 0.f;
-                part[r] = update_lane<NC>(v[r], dA, dtv * xr, bb, cc);
+                part[r] = update_row<RPW, NC, ST>(v[r], dA, dtv * xr, bb, cc);
                 if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
             }
             const float total = reduce_rows<RPW>(part, lane);
