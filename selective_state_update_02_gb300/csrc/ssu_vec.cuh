@@ -31,8 +31,8 @@ __device__ __forceinline__ void load_bc_vec(const __nv_bfloat16 *p, float (&o)[N
     }
 }
 
-// Two ways of forming the per-row inputs, chosen per instantiation from a same-box A/B at batch
-// 128 (and 8 / 512 for fp32 at dstate 128), since the compiler's schedules differ:
+// Per-instantiation forms of the per-row work, each chosen from a same-box A/B at batch 128
+// (and 8 / 512 for fp32 at dstate 128), since the compiler's schedules differ:
 //  * kShuffleK: lane r < RPW loads x of row r and forms dt * x there; the other lanes get the
 //    product by a shuffle (instead of every lane loading every row's x and multiplying).  On
 //    for a bf16 state (dstate 128: 14.88 -> 13.78 us; 64: 11.91 -> 10.72) and for fp32 with 8
