@@ -58,19 +58,37 @@ bool launch_shape_ok(const ssu_launch_t &l) {
 
 namespace {
 
-// Built-in launch-shape table, from the cold-L2 sweeps on GB300 (bench.py --sweep, with and
-// without --dstate / --state-dtype).  The VEC kernel with 8 rows per warp and 2 warps per CTA
-// is fastest from batch 32 up (an fp32 state at dstate 256: 4 rows per warp, fewer
-// registers; 16 rows per warp is slower in every bucket).  A call too small to give every SM
-// 16 warps at that size steps down to 4, then 2 rows per warp with 4 warps per CTA (batch 8:
-// 3.80 us instead of 3.97).  The tile never exceeds the headdim.
+// Built-in launch-shape table, from the cold-L2 sweeps on GB300 (bench.py --sweep with and
+// without --dstate / --state-dtype, batch 1 to 512, 16 heads, headdim 64), keyed by the bytes
+// of one state row.  A small call gives each warp about 1 KiB of state (2 rows of 512 B, 4 of
+// 256 B; 2 rows at 128 B and 1 KiB) in CTAs of 4 warps; from a size on, 8 rows per warp (4 for
+// 1 KiB rows), in CTAs of 4 warps (2 for a bf16 state of 256 or 512 B rows, and for 1 KiB
+// rows).  The size is counted in state rows per call, for 152 SMs: 4,096 rows of 128 B, 32,768
+// of 256 B, 16,384 of 512 B or 1 KiB (batch 4 / 32 / 16 / 16 at 16 heads of 64 rows).  Against
+// the earlier table (8 rows x 2 warps, stepping down to 4 and 2 rows below 16 warps per SM),
+// e.g. batch 16: fp32 dstate 128 5.02 -> 4.51 us, fp32 dstate 64 3.98 -> 3.30, bf16 dstate 64
+// 4.01 -> 2.78, bf16 dstate 128 4.20 -> 3.42; bf16 dstate 64 at batch 128: 10.41 -> 9.29; fp32
+// dstate 128 at batch 128: 22.25 -> 22.17.  16 rows per warp is slower in every bucket.  The
+// tile never exceeds the headdim.
 ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
     (void)st;
-    int rpw = s.dstate == 256 && s.state_dtype == SSU_STATE_F32 ? 4 : 8;
+    const bool bf16 = s.state_dtype == SSU_STATE_BF16;
+    const long long row_bytes = s.dstate * (bf16 ? 2 : 4);
     const long long rows = s.batch * s.nheads * s.headdim;
-    while (rpw > 2 && rows / rpw < 16LL * hd.sm_count) rpw >>= 1;
+    const long long large_from = row_bytes <= 128 ? 4096 : row_bytes <= 256 ? 32768 : 16384;
+    const bool large = rows * 152 >= large_from * hd.sm_count;
+    int rpw, wpc;
+    if (row_bytes >= 1024) {
+        rpw = large ? 4 : 2;
+        wpc = large ? 2 : 4;
+    } else if (large) {
+        rpw = 8;
+        wpc = bf16 && row_bytes >= 256 ? 2 : 4;
+    } else {
+        rpw = row_bytes == 256 ? 4 : 2;
+        wpc = 4;
+    }
     while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
-    int wpc = rpw <= 2 ? 4 : 2;
     while (wpc > 1 && rpw * wpc > s.headdim) wpc >>= 1;
     return ssu_launch_t{SSU_MODE_VEC, rpw, wpc, 0};
 }
