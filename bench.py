@@ -47,7 +47,6 @@ FALLBACK_HBM_GBS = 6800.0
 PAGE_US = {8: 4.02, 128: 24.1, 512: 85.7}   # sglang PR #41223 Speedup Result, B200 (context)
 CSRC = ROOT / "selective_state_update_02_gb300" / "csrc"
 KERNEL_SOURCES = [CSRC / "ssu_vec.cuh", CSRC / "ssu_device.cuh"]     # VEC kernel
-BULK_SOURCES = [CSRC / "ssu_bulk.cuh", CSRC / "ssu_device.cuh"]      # BULK kernel
 TOKENS_SOURCES = [CSRC / "ssu_tokens.cuh", CSRC / "ssu_device.cuh"]  # multi-token kernel
 COPY_SOURCES = [CSRC / "ssu_copy.cu", CSRC / "ssu_device.cuh"]       # block-copy kernels
 
@@ -98,14 +97,14 @@ def source_digest(files=None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_tag: str, bulk: bool = False, sources=None) -> int | None:
+def recorded_traffic(workload_tag: str, sources=None) -> int | None:
     """DRAM bytes per launch from a committed ncu summary, if it was taken on this source.
 
     The summaries under profiles/ carry a line
     ``traffic_per_launch_bytes: <int> source: <digest> workload: <tag>``.  The digest covers
-    ``sources`` (default: the VEC kernel's, or the BULK kernel's with ``bulk``).
+    ``sources`` (default: the VEC kernel's).
     """
-    digest = source_digest(sources or (BULK_SOURCES if bulk else KERNEL_SOURCES))
+    digest = source_digest(sources or KERNEL_SOURCES)
     for f in sorted((ROOT / "profiles").glob("*.md")):
         for m in re.finditer(r"traffic_per_launch_bytes:\s*(\d+)\s+source:\s*([0-9a-f]+)\s+"
                              r"workload:\s*(\S+)", f.read_text()):
@@ -247,10 +246,13 @@ class Workload:
             raise ssu.SsuError(st, "ssu_update", ssu.last_error())
 
 
-def time_calls(wl_, handle, steps: int, warmup: int, clocks_gpu: int | None = None):
-    """Warm up, then time exactly `steps` calls replayed from CUDA graphs.
+def time_calls(wl_, handle, steps: int, warmup: int, clocks_gpu: int | None = None,
+               repeats: int = 1, barrier=None):
+    """Warm up, then time exactly `steps` calls replayed from CUDA graphs, `repeats` times
+    (each repeat bracketed by `barrier` (if any), a device synchronisation and CUDA events on
+    the launching stream).
 
-    Returns (elapsed_ms, untimed_calls, clocks).
+    Returns (elapsed_ms per repeat, untimed_calls, clocks).
     """
     import torch
     stream = torch.cuda.Stream()
@@ -276,27 +278,34 @@ def time_calls(wl_, handle, steps: int, warmup: int, clocks_gpu: int | None = No
             g.replay()
             untimed += n
     stream.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(clocks_gpu) if clocks_gpu is not None else None
     if sampler:
         sampler.__enter__()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        if full:
-            g, _ = graphs[0]
-            for _ in range(full):
-                g.replay()
-        if rem:
-            graphs[-1][0].replay()
-        ev1.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
+    times = []
+    for _ in range(repeats):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if barrier is not None:
+            barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            if full:
+                g, _ = graphs[0]
+                for _ in range(full):
+                    g.replay()
+            if rem:
+                graphs[-1][0].replay()
+            ev1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        if barrier is not None:
+            barrier()
+        times.append(ev0.elapsed_time(ev1))
     clocks = None
     if sampler:
         sampler.__exit__(None, None, None)
         clocks = sampler.result()
-    return ev0.elapsed_time(ev1), untimed, clocks
+    return times, untimed, clocks
 
 
 def time_e2e(wl_, handle, steps: int, dev) -> dict:
@@ -475,35 +484,46 @@ class OracleCall:
         self.x, self.dt, self.B, self.C = wl.request_inputs(rng, bs, H, N=N)
         self.bs = bs
         self.threads = os.cpu_count() or 1
+        self.pool = self.pool0.copy()
 
     def run(self, requests: int | None = None) -> float:
-        """Seconds for one call over the first `requests` requests (all by default)."""
+        """Seconds of one oracle call over the first `requests` requests (all by default),
+        timed around the call alone; the pool is refreshed from its initial copy outside the
+        timed region (the state values only drift, so each call does the same work)."""
         n = self.bs if requests is None else max(1, min(self.bs, requests))
-        pool = self.pool0.copy()
+        np.copyto(self.pool, self.pool0)
         t0 = time.perf_counter()
-        self.oracle.ssu_step_inplace(pool, self.idx[:n], self.x[:n], self.dt[:n], self.dt_bias,
-                                     self.A, self.B[:n], self.C[:n], self.D,
+        self.oracle.ssu_step_inplace(self.pool, self.idx[:n], self.x[:n], self.dt[:n],
+                                     self.dt_bias, self.A, self.B[:n], self.C[:n], self.D,
                                      threads=self.threads)
         return time.perf_counter() - t0
 
 
+def oracle_call_us(oc: OracleCall, calls: int, requests: int, warmup: int = 1) -> tuple:
+    """The oracle's µs per full-batch call: `warmup` untimed calls, then `calls` timed calls
+    over `requests` requests each, scaled by bs / requests; (median, per-call list).  The
+    reference arm and the cpu_baseline leg both time the oracle with this one routine."""
+    for _ in range(warmup):
+        oc.run(requests)
+    per = [oc.run(requests) * (oc.bs / requests) * 1e6 for _ in range(calls)]
+    return statistics.median(per), per
+
+
 def cpu_baseline(bs: int, H: int, budget_s: float = 12.0, N: int = DSTATE) -> dict:
     oc = OracleCall(bs, H, seed=7, N=N)
-    oc.run()
-    times = []
-    t_start = time.perf_counter()
-    while time.perf_counter() - t_start < budget_s and len(times) < 50:
-        times.append(oc.run())
-    med = statistics.median(times)
+    t_full = oc.run()
+    calls = int(max(3, min(50, budget_s / max(t_full, 1e-6))))
+    med, per = oracle_call_us(oc, calls, bs)
     # the same oracle on one thread, over a quarter of the batch (scaled to the full call)
     threads, oc.threads = oc.threads, 1
     quarter = max(1, bs // 4)
-    single = [oc.run(quarter) * (bs / quarter) for _ in range(3)]
+    single, _ = oracle_call_us(oc, 3, quarter)
     oc.threads = threads
-    return {"value": round(med * 1e6, 1), "unit": UNIT, "cores": oc.threads, "kind": "oracle",
-            "sample": f"{len(times)} full calls (batch {bs}, {H} heads, headdim 64, dstate {N}) "
-                      f"of the fp64 C oracle split over {oc.threads} host threads; median",
-            "single_thread_value": round(statistics.median(single) * 1e6, 1),
+    return {"value": round(med, 1), "unit": UNIT, "cores": oc.threads, "kind": "oracle",
+            "sample": f"{calls} full calls (batch {bs}, {H} heads, headdim 64, dstate {N}) "
+                      f"of the fp64 C oracle split over {oc.threads} host threads (one "
+                      f"persistent pool), each timed around the call alone; median",
+            "single_thread_value": round(single, 1),
             "single_thread_sample": f"3 calls over {quarter} of the {bs} requests on one "
                                     f"thread, scaled to the full batch; median"}
 
@@ -573,6 +593,10 @@ def dist_env():
 
 
 def run_reference(args) -> None:
+    """The reference arm: the fp64 oracle on the host cores, timed by the routine the
+    cpu_baseline leg uses (oracle_call_us); each step is one oracle call over a sample of the
+    requests sized so the whole run stays within about two minutes, scaled to the full
+    batch; the median step is reported."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -582,13 +606,7 @@ def run_reference(args) -> None:
     budget = 120.0
     total = args.steps + args.warmup
     req = max(1, min(bs, int(bs * budget / max(total * t_full, 1e-9))))
-    for _ in range(args.warmup):
-        oc.run(req)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oc.run(req)
-    per_step = (time.perf_counter() - t0) / args.steps
-    value = per_step * (bs / req) * 1e6
+    value, per = oracle_call_us(oc, args.steps, req, warmup=args.warmup)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -598,24 +616,51 @@ def run_reference(args) -> None:
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oc.threads,
                          "kind": "oracle",
                          "sample": f"each step: the fp64 C oracle on {req} of {bs} requests "
-                                   f"({H} heads) over {oc.threads} host threads, scaled to the "
-                                   f"full batch"},
+                                   f"({H} heads) over {oc.threads} host threads (one "
+                                   f"persistent pool), timed around the call alone and scaled "
+                                   f"to the full batch; median of {args.steps} steps"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def config_for(bs: int, n_sets: int, N: int = DSTATE, state_dtype: str = "f32") -> dict:
+def config_for(bs: int, n_sets: int, N: int = DSTATE, state_dtype: str = "f32",
+               H: int = NHEADS) -> dict:
     eb = 2 if state_dtype == "bf16" else 4
-    return {"workload": f"decode step, batch {bs}, {NHEADS} heads, headdim {HEADDIM}, dstate "
+    return {"workload": f"decode step, batch {bs}, {H} heads, headdim {HEADDIM}, dstate "
                         f"{N}, {state_dtype} state pool of {bs * n_sets} slots in {n_sets} "
                         f"disjoint {bs}-slot rotation sets; x/B/C strided views of one packed "
                         f"bf16 tensor, dt/A/D/dt_bias stride-0 broadcasts",
-            "batch": bs, "nheads": NHEADS, "headdim": HEADDIM, "dstate": N,
+            "batch": bs, "nheads": H, "headdim": HEADDIM, "dstate": N,
             "state_dtype": state_dtype, "ngroups": NGROUPS, "pool_slots": bs * n_sets,
             "l2": f"inputs larger than L2: call i touches set i mod {n_sets}; the sets hold "
-                  f"{bs * n_sets * NHEADS * HEADDIM * N * eb / 2 ** 20:.0f} MiB of state"}
+                  f"{bs * n_sets * H * HEADDIM * N * eb / 2 ** 20:.0f} MiB of state"}
+
+
+REPEATS = 5  # timed repeats per measurement; the median is reported (the pages' protocol)
+
+
+def median_call_us(wl_, handle, steps: int, warmup: int, repeats: int = REPEATS) -> tuple:
+    """(median µs per call over `repeats` timed runs of `steps` calls, per-repeat µs/call)."""
+    ms, _, _ = time_calls(wl_, handle, steps, warmup, repeats=repeats)
+    per = [m * 1000.0 / steps for m in ms]
+    return statistics.median(per), per
+
+
+def batch_line(b: int, handle, dev, l2: int, steps: int, warmup: int, H: int = NHEADS,
+               seed: int = 0) -> dict:
+    """µs per call (median of REPEATS runs of `steps` calls) and TB/s of one batch size."""
+    import torch
+    w = Workload(b, H, dev, seed=seed, l2_bytes=l2)
+    us, per = median_call_us(w, handle, steps, warmup)
+    rec = {"us_per_call": round(us, 3),
+           "tbps": round(bytes_per_call(b, H=H) / (us * 1e-6) / 1e12, 3),
+           "steps": steps, "repeats": len(per), "repeat_us": [round(v, 3) for v in per],
+           "sets": w.n_sets}
+    del w
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_ours(args) -> None:
@@ -634,7 +679,7 @@ def run_ours(args) -> None:
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     handle = ssu.ssu_create(local)
     if args.launch:
-        ssu.ssu_set_launch(handle, *[int(v) for v in args.launch.split(",")])
+        ssu.ssu_set_launch_override(handle, args.launch)
     ssu.ssu_set_pdl(handle, not args.no_pdl)
     warmup = max(args.warmup, 3)
     bs = args.batch
@@ -648,23 +693,28 @@ def run_ours(args) -> None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    barrier()
-    ms, untimed, clocks = time_calls(main, handle, args.steps, warmup, clocks_gpu=_smi_index(local))
-    barrier()
-    per_rank = gather_elapsed(ms * 1000.0, world, dev)
-    value = aggregate_value(per_rank, args.steps)
-    per_launch_us = max(per_rank) / args.steps
+    # The headline: REPEATS timed runs of exactly `steps` calls, each bracketed by a barrier
+    # and a device synchronisation; per run the slowest rank's time; the median run reported.
+    ms, untimed, clocks = time_calls(main, handle, args.steps, warmup,
+                                     clocks_gpu=_smi_index(local), repeats=REPEATS,
+                                     barrier=barrier)
+    runs = [max(gather_elapsed(m * 1000.0, world, dev)) for m in ms]
+    slowest = statistics.median(runs)
+    value = aggregate_value([slowest] * world, args.steps)
+    per_launch_us = slowest / args.steps
     peaks = load_peaks()
     bpc = bytes_per_call(bs, N=N, state_bytes=eb)
     achieved_gbs = bpc / (per_launch_us * 1e-6) / 1e9
     launch = ssu.ssu_get_launch(handle, main.args[0][1])
-    tag = f"batch{bs}" + ("-bulk" if launch[0] == 2 else "")
+    tag = f"batch{bs}"
     if not default_workload:
         tag += f"-n{N}-{sdt}"
-    traffic = recorded_traffic(tag, bulk=launch[0] == 2)
+    traffic = recorded_traffic(tag)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": warmup, "untimed_calls": untimed,
+        "steps": args.steps, "warmup": warmup, "repeats": REPEATS,
+        "repeat_us_per_call": [round(r / args.steps, 3) for r in runs],
+        "untimed_calls": untimed,
         "ms_per_step": round(value / 1000.0, 6),
         "higher_is_better": False, "scaling": "weak",
         "vs_baseline": (round(value / PAGE_US[bs], 4)
@@ -675,7 +725,8 @@ def run_ours(args) -> None:
         "config": config_for(bs, main.n_sets, N, sdt) | {
             "launch": {"mode": launch[0], "rows_per_warp": launch[1],
                        "warps_per_cta": launch[2], "stages": launch[3],
-                       "programmatic_dependent_launch": not args.no_pdl}},
+                       "programmatic_dependent_launch": not args.no_pdl},
+            "timing": f"median of {REPEATS} timed runs of {args.steps} graph-replayed calls"},
         "achieved_tbps": round(achieved_gbs / 1000.0, 3),
         "pct_of_nominal_8tbps": round(100.0 * achieved_gbs / NOMINAL_HBM_GBS, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1),
@@ -683,8 +734,8 @@ def run_ours(args) -> None:
                      "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": bpc,
                      "peak_source": peaks["source"],
-                     "kernel": "ssu_bulk_kernel" if launch[0] == 2 else "ssu_vec_kernel"},
-        "gpu_launches": args.steps,
+                     "kernel": "ssu_vec_kernel"},
+        "gpu_launches": args.steps * REPEATS,
         "clocks": clocks,
     }
     if not args.skip_ceiling:
@@ -695,22 +746,23 @@ def run_ours(args) -> None:
         line["roofline"]["frac_of_same_size_inplace"] = round(
             (2 * state_bytes / (per_launch_us * 1e-6) / 1e9) / ceil_gbs, 4)
     if not args.skip_extra and world == 1 and default_workload:
-        by = {}
+        # Batches 8, 128 and 512, each over at least 2000 calls per run (the headline above
+        # runs exactly `steps`); then the same with programmatic dependent launch off.
+        by, no_pdl = {}, {}
         for b in (8, 128, 512):
-            if b == bs:
-                by[str(b)] = {"us_per_call": round(per_launch_us, 3),
-                              "tbps": round(achieved_gbs / 1000.0, 3)}
-                continue
-            w = Workload(b, NHEADS, dev, seed=100 + b, l2_bytes=l2)
             n = max(2000, min(args.steps, int(2e5 / max(b, 1))))
-            ms_b, _, _ = time_calls(w, handle, n, warmup)
-            us = ms_b * 1000.0 / n
-            by[str(b)] = {"us_per_call": round(us, 3),
-                          "tbps": round(bytes_per_call(b) / (us * 1e-6) / 1e12, 3),
-                          "pages_b200_us": PAGE_US[b], "steps": n}
-            del w
-            torch.cuda.empty_cache()
+            by[str(b)] = batch_line(b, handle, dev, l2, n, warmup, seed=100 + b) | {
+                "pages_b200_us": PAGE_US[b]}
         line["by_batch"] = by
+        ssu.ssu_set_pdl(handle, False)
+        for b in (8, 128, 512):
+            n = max(2000, min(args.steps, int(2e5 / max(b, 1))))
+            no_pdl[str(b)] = batch_line(b, handle, dev, l2, n, warmup, seed=100 + b)
+        ssu.ssu_set_pdl(handle, not args.no_pdl)
+        line["no_pdl"] = no_pdl | {
+            "note": "the same calls launched without programmatic dependent launch "
+                    "(ssu_set_pdl(h, 0)): each call starts only after the previous one has "
+                    "completed"}
     if not args.skip_e2e:
         line["e2e"] = time_e2e(main, handle, min(args.steps, args.e2e_steps), dev)
     if rank == 0 and world == 1 and not args.skip_cpu:
@@ -720,6 +772,49 @@ def run_ours(args) -> None:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_head_sweep(args) -> None:
+    """The head-count sweep workload: H = 8, 32, 64, 128 at batch 256, headdim 64, dstate
+    128, fp32 state, a pool of at least 3x L2 with random non-contiguous indices; one JSON
+    line per head count."""
+    import torch
+
+    import selective_state_update_02_gb300 as ssu
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = ssu.ssu_create(0)
+    ssu.ssu_set_pdl(handle, not args.no_pdl)
+    peaks = load_peaks()
+    bs = 256
+    warmup = max(args.warmup, 3)
+    for H in args.heads:
+        w = Workload(bs, H, dev, seed=300 + H, l2_bytes=l2, packed=True)
+        n = max(400, min(args.steps, int(4e5 / H)))
+        us, per = median_call_us(w, handle, n, warmup)
+        bpc = bytes_per_call(bs, H=H)
+        gbs = bpc / (us * 1e-6) / 1e9
+        launch = ssu.ssu_get_launch(handle, w.args[0][1])
+        rec = {"metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": 1,
+               "steps": n, "warmup": warmup, "repeats": len(per),
+               "repeat_us_per_call": [round(v, 3) for v in per],
+               "higher_is_better": False, "dtype": "f32", "data": "synthetic",
+               "config": config_for(bs, w.n_sets, H=H) | {
+                   "launch": {"rows_per_warp": launch[1], "warps_per_cta": launch[2],
+                              "programmatic_dependent_launch": not args.no_pdl}},
+               "achieved_tbps": round(gbs / 1000.0, 3),
+               "pct_of_nominal_8tbps": round(100.0 * gbs / NOMINAL_HBM_GBS, 1),
+               "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(gbs / peaks["hbm_gbs"], 4),
+                            "traffic": recorded_traffic(f"heads{H}-batch{bs}"),
+                            "algorithmic_bytes_per_launch": bpc,
+                            "peak_source": peaks["source"], "kernel": "ssu_vec_kernel"}}
+        print(json.dumps(rec), flush=True)
+        del w
+        torch.cuda.empty_cache()
+    assert ssu.ssu_get_error(handle) == (0, -1)
+    ssu.ssu_destroy(handle)
 
 
 def _smi_index(local: int) -> int:
@@ -854,10 +949,8 @@ def run_copy(args) -> None:
     reqs_list = tuple(args.copy_reqs)
     if args.sweep:
         reqs_list = (8, 32, 128)
-        shapes = ([(ssu.SSU_COPY_VEC, c, v, t) for c in (16, 32, 64) for v in (4, 8, 16)
-                   for t in (128, 256)] +
-                  [(ssu.SSU_COPY_BULK, c, st, 0) for c in (16, 32, 64) for st in (3, 4, 6)
-                   if 128 + st * c * 1024 <= 220 * 1024])
+        shapes = [(ssu.SSU_COPY_VEC, c, v, t) for c in (16, 32, 64) for v in (4, 8, 16)
+                  for t in (128, 256)]
     cpu_copy = None
     for reqs in reqs_list:
         w = CopyWorkload(reqs, dev, l2)
@@ -1020,10 +1113,14 @@ def run_tokens(args) -> None:
     ssu.ssu_destroy(handle)
 
 
-SWEEP_SHAPES = ([(1, r, w, 0) for r in (1, 2, 4, 8, 16) for w in (1, 2, 4, 8)] +
-                [(2, r, w, st) for r, w in ((4, 4), (8, 2), (8, 4), (16, 2), (16, 4), (8, 8),
-                                            (4, 8), (2, 8))
-                 for st in (2, 3, 4, 6) if st * r * w * 512 <= 200 * 1024])
+def sweep_shapes(N: int, state_dtype: str) -> list[tuple[int, int, int, int]]:
+    """Every launch shape of the bucket: rows per warp = rows per vector instruction x
+    {1, 2, 4, 8} (and 16 for an fp32 state of dstate 128), 1 to 8 warps per CTA."""
+    rpi = max(1, 512 // (N * (2 if state_dtype == "bf16" else 4)))
+    rows = [rpi * k for k in (1, 2, 4, 8)]
+    if N == DSTATE and state_dtype == "f32":
+        rows.append(16)
+    return [(1, r, w, 0) for r in rows for w in (1, 2, 4, 8)]
 
 
 def run_sweep(args) -> None:
@@ -1040,15 +1137,12 @@ def run_sweep(args) -> None:
         N, sdt = args.dstate, args.state_dtype
         eb = 2 if sdt == "bf16" else 4
         w = Workload(bs, NHEADS, dev, seed=200 + bs, l2_bytes=l2, N=N, state_dtype=sdt)
-        shapes = SWEEP_SHAPES
-        if N != DSTATE or sdt != "f32":   # BULK and 16 rows per warp: fp32, dstate 128 only
-            shapes = [sh for sh in SWEEP_SHAPES if sh[0] == 1 and sh[1] <= 8]
+        shapes = sweep_shapes(N, sdt)
         n = max(1000, int(args.sweep_us_budget / (0.16 * bs + 2.0)))
         for mode, rpw, wpc, stages in shapes:
             ssu.ssu_set_launch(handle, mode, rpw, wpc, stages)
-            ms, _, _ = time_calls(w, handle, n, 5)
-            us = ms * 1000.0 / n
-            rec = {"batch": bs, "mode": "vec" if mode == 1 else "bulk", "rows_per_warp": rpw,
+            us, _ = median_call_us(w, handle, n, 5, repeats=3)
+            rec = {"batch": bs, "mode": "vec", "rows_per_warp": rpw,
                    "warps_per_cta": wpc, "stages": stages, "us_per_call": round(us, 3),
                    "tbps": round(bytes_per_call(bs, N=N, state_bytes=eb) / (us * 1e-6) / 1e12, 3),
                    "steps": n, "dstate": N, "state_dtype": sdt}
@@ -1056,8 +1150,7 @@ def run_sweep(args) -> None:
             if bs not in best or us < best[bs]["us_per_call"]:
                 best[bs] = rec
         ssu.ssu_set_launch(handle, ssu.SSU_MODE_AUTO)
-        ms, _, _ = time_calls(w, handle, n, 5)
-        us = ms * 1000.0 / n
+        us, _ = median_call_us(w, handle, n, 5, repeats=3)
         launch = ssu.ssu_get_launch(handle, w.args[0][1])
         print(json.dumps({"batch": bs, "mode": "table", "launch": launch,
                           "us_per_call": round(us, 3)}), flush=True)
@@ -1073,7 +1166,12 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--batch", type=int, default=DEFAULT_BATCH, choices=[8, 128, 512])
+    ap.add_argument("--batch", type=int, default=DEFAULT_BATCH,
+                    help="requests per call (the pages' workloads: 8, 128, 512)")
+    ap.add_argument("--head-sweep", action="store_true",
+                    help="the head-count sweep instead: H = --heads at batch 256")
+    ap.add_argument("--heads", type=int, nargs="+", default=[8, 32, 64, 128],
+                    help="head counts timed by --head-sweep")
     ap.add_argument("--dstate", type=int, default=DSTATE, choices=[64, 128, 256])
     ap.add_argument("--state-dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--e2e-steps", type=int, default=5000)
@@ -1081,8 +1179,8 @@ def main() -> None:
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--launch", default="",
-                    help="force a launch shape 'mode,rows_per_warp,warps_per_cta,stages' "
-                         "(mode 1 = VEC, 2 = BULK) instead of the built-in table")
+                    help="force a launch shape 'rows_per_warp,warps_per_cta' (the string "
+                         "ssu_set_launch_override takes) instead of the built-in table")
     ap.add_argument("--tokens", action="store_true",
                     help="multi-token step (T = 1..4) at --batch instead")
     ap.add_argument("--copy", action="store_true",
@@ -1107,6 +1205,8 @@ def main() -> None:
     args = ap.parse_args()
     if args.steps < 1:
         raise SystemExit("--steps must be >= 1")
+    if args.batch < 1:
+        raise SystemExit("--batch must be >= 1")
     if args.tokens:
         run_tokens(args)
     elif args.copy:
@@ -1115,6 +1215,8 @@ def main() -> None:
         run_calibrate(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.head_sweep:
+        run_head_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     elif args.e2e_only:

@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-#define SSU_ABI_VERSION 1
+#define SSU_ABI_VERSION 2
 
 /* Opaque per-device context: holds the device error counters and the launch-shape choice. */
 typedef struct ssu_handle_s *ssu_handle_t;
@@ -59,9 +59,7 @@ typedef enum {
     SSU_ERR_UNSUPPORTED = 2, /* a size or stride form this build does not implement */
     SSU_ERR_MISALIGNED = 3,  /* state_pool base or a state stride not a multiple of 16 bytes */
     SSU_ERR_CUDA = 4,        /* a CUDA runtime call failed; ssu_last_error() names it */
-    SSU_ERR_INDEX_OOB = 5,   /* ssu_get_error: at least one request was skipped */
-    SSU_ERR_TIMEOUT = 6      /* ssu_get_error: a BULK pipeline wait gave up after 1 s; the
-                                call's results are incomplete (never expected; a defect) */
+    SSU_ERR_INDEX_OOB = 5    /* ssu_get_error: at least one request was skipped */
 } ssu_status_t;
 
 typedef enum { SSU_INDEX_I32 = 0, SSU_INDEX_I64 = 1 } ssu_index_dtype_t;
@@ -103,21 +101,16 @@ typedef struct {
 /* Launch shapes of the streaming kernel. */
 typedef enum {
     SSU_MODE_AUTO = 0,   /* use the built-in table (the default) */
-    SSU_MODE_VEC = 1,    /* one CTA per tile; 16-byte vector loads/stores through registers */
-    SSU_MODE_BULK = 2    /* persistent CTAs; bulk asynchronous copies (TMA engine) of whole
-                            tiles through a ring of shared-memory stages.  fp32 state, dstate
-                            128, contiguous rows (row stride == dstate) only; a forced BULK
-                            shape returns SSU_ERR_UNSUPPORTED otherwise */
+    SSU_MODE_VEC = 1     /* one CTA per tile; 16-byte vector loads/stores through registers */
 } ssu_mode_t;
 
 /* A tile is rows_per_warp * warps_per_cta consecutive state rows of one (request, head). */
 typedef struct {
     int32_t mode;          /* ssu_mode_t */
-    int32_t rows_per_warp; /* rows each warp updates per tile: VEC 1,2,4,8 (16 for an fp32
-                              state of dstate 128); BULK 2,4,8,16 */
-    int32_t warps_per_cta; /* VEC: 1..16 warps; BULK: 1..8 compute warps (plus one producer) */
-    int32_t stages;        /* BULK: shared-memory ring depth, 2..8 (stages x tile <= the
-                              device's shared memory per CTA); VEC: ignored */
+    int32_t rows_per_warp; /* rows each warp updates per tile: 1, 2, 4 or 8 (16 for an fp32
+                              state of dstate 128) */
+    int32_t warps_per_cta; /* 1..16 warps */
+    int32_t stages;        /* reserved: ignored (write 0) */
 } ssu_launch_t;
 
 /* ABI version this library was built with (SSU_ABI_VERSION). */
@@ -208,8 +201,7 @@ ssu_status_t ssu_update_from_host(ssu_handle_t handle, void *state_pool,
  * Synchronise `stream`, then read and clear the handle's device counters.
  * *skipped receives the number of requests skipped since the last read (may be NULL);
  * *first_bad receives the smallest skipped request index b, or -1 (may be NULL).
- * Returns SSU_ERR_TIMEOUT if a BULK pipeline wait gave up, else SSU_ERR_INDEX_OOB when
- * *skipped > 0, SSU_OK otherwise.
+ * Returns SSU_ERR_INDEX_OOB when *skipped > 0, SSU_OK otherwise.
  */
 ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *skipped,
                            int64_t *first_bad);
@@ -231,6 +223,16 @@ ssu_status_t ssu_check_indices(const void *host_indices, int64_t n, int32_t inde
  */
 ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch);
 
+/*
+ * The same override written as text, for a configuration file or the environment:
+ * "rows_per_warp,warps_per_cta" (for example "8,4"), optionally prefixed by the mode name
+ * ("vec,8,4").  NULL, "" or "auto" restores the built-in table.  A spec that does not parse,
+ * or names a shape ssu_set_launch would refuse, returns SSU_ERR_INVALID_ARG /
+ * SSU_ERR_UNSUPPORTED and leaves the handle's choice unchanged.  ssu_create applies the
+ * environment variable SSU_LAUNCH, when set, in the same way (and fails if it does not parse).
+ */
+ssu_status_t ssu_set_launch_override(ssu_handle_t handle, const char *spec);
+
 /* The launch shape ssu_update would use for `shape` on this handle (table or override). */
 ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
                             ssu_launch_t *launch);
@@ -243,8 +245,8 @@ ssu_status_t ssu_get_launch(ssu_handle_t handle, const ssu_shape_t *shape,
  * each CTA releases its own dependents once its stores are issued.  This hides part of the
  * launch gap between back-to-back kernels (batch 8: 3.75 -> 3.38 us per call).  Work other
  * than a kernel (a copy, an event wait) still completes before the launch starts, as in any
- * stream.  The VEC block copy (ssu_copy_blocks) follows the same setting; BULK launches (of
- * the decode step and of the copy) and the allocation-free entry point never use it.
+ * stream.  The block copy (ssu_copy_blocks) follows the same setting; the allocation-free
+ * entry point never uses it.
  */
 ssu_status_t ssu_set_pdl(ssu_handle_t handle, int32_t enable);
 
@@ -312,16 +314,14 @@ typedef struct {
 
 typedef enum {
     SSU_COPY_AUTO = 0,  /* built-in choice */
-    SSU_COPY_VEC = 1,   /* 16-byte vector loads and stores through registers */
-    SSU_COPY_BULK = 2   /* bulk asynchronous copies (TMA engine) through shared memory */
+    SSU_COPY_VEC = 1    /* 16-byte vector loads and stores through registers */
 } ssu_copy_mode_t;
 
 typedef struct {
     int32_t mode;        /* ssu_copy_mode_t */
     int32_t chunk_kib;   /* bytes per work item, KiB: 4, 8, 16, 32 or 64 */
-    int32_t stages;      /* BULK: shared-memory ring depth, 2..8; VEC: 16-byte vectors per thread
-                            per pass, 1..16 */
-    int32_t threads;     /* VEC: threads per CTA, 32..256 (multiple of 32); BULK: ignored */
+    int32_t stages;      /* 16-byte vectors per thread per pass: 1, 2, 4, 8 or 16 */
+    int32_t threads;     /* threads per CTA, 32..256 (multiple of 32) */
 } ssu_copy_launch_t;
 
 /*
@@ -354,12 +354,15 @@ ssu_status_t ssu_copy_set_launch(ssu_handle_t handle, const ssu_copy_launch_t *l
  * Arguments are those of ssu_update, on the CURRENT CUDA device, plus:
  *   counters_out  optional caller-owned DEVICE buffer of 3 uint32: after the kernel the call
  *                 enqueues a copy of [skipped requests, smallest skipped request index
- *                 (0xFFFFFFFF if none), 0]; NULL skips the copy.
+ *                 (0xFFFFFFFF if none), 0 (reserved)]; NULL skips the copy.
  * Each call clears the shared counters, launches the VEC kernel of the built-in table and
- * copies the counters out, all on `stream`.  The first call on a device looks up the
- * array's device address (once per device, with that device current); make that first call
- * before any stream capture.  Every call on a device shares the one array: calls that
- * overlap on the GPU (different streams, no ordering) race on the counters, so order them.
+ * copies the counters out, all on `stream`.  Every call looks up the array's device address
+ * on the current device (cudaGetSymbolAddress, with that device current) and fails with
+ * SSU_ERR_CUDA if the lookup does; nothing is cached, so the address stays right after a
+ * device reset.  The first call on a device also loads the library's device code there: make
+ * that first call before any stream capture.  Every call on a device shares the one array:
+ * calls that overlap on the GPU (different streams, no ordering) race on the counters, so
+ * order them.
  * Batches above SSU_STATIC_MAX_BATCH requests are rejected with SSU_ERR_UNSUPPORTED (the
  * smallest skipped index is kept in one 32-bit word of the array).  Never calls cudaMalloc,
  * cudaFree or any allocating routine.

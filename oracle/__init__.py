@@ -59,6 +59,19 @@ def _load():
     return _lib
 
 
+_executors: dict = {}
+
+
+def _executor(threads: int):
+    """One thread pool per thread count, kept for the life of the process (ctypes releases
+    the interpreter lock while the C step runs, so the chunks run in parallel)."""
+    ex = _executors.get(threads)
+    if ex is None:
+        from concurrent.futures import ThreadPoolExecutor
+        ex = _executors[threads] = ThreadPoolExecutor(threads)
+    return ex
+
+
 def _ptr(a: np.ndarray, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
@@ -117,11 +130,9 @@ def ssu_step_inplace(pool64: np.ndarray, idx, x, dt, dt_bias, A, B, C, D,
     if threads <= 1 or bs < 2:
         skipped = run(0, bs)
     else:
-        from concurrent.futures import ThreadPoolExecutor
         cuts = np.linspace(0, bs, min(threads, bs) + 1).astype(int)
-        with ThreadPoolExecutor(len(cuts) - 1) as ex:
-            parts = list(ex.map(lambda i: run(int(cuts[i]), int(cuts[i + 1])),
-                                range(len(cuts) - 1)))
+        parts = list(_executor(threads).map(lambda i: run(int(cuts[i]), int(cuts[i + 1])),
+                                            range(len(cuts) - 1)))
         skipped = -1 if min(parts) < 0 else sum(parts)
     if skipped < 0:
         raise ValueError("oracle rejected the shape")

@@ -29,7 +29,6 @@ SSU_ERR_UNSUPPORTED = 2
 SSU_ERR_MISALIGNED = 3
 SSU_ERR_CUDA = 4
 SSU_ERR_INDEX_OOB = 5
-SSU_ERR_TIMEOUT = 6
 
 SSU_INDEX_I32 = 0
 SSU_INDEX_I64 = 1
@@ -39,7 +38,6 @@ SSU_STATE_BF16 = 1
 
 SSU_MODE_AUTO = 0
 SSU_MODE_VEC = 1
-SSU_MODE_BULK = 2
 
 _i64 = ctypes.c_int64
 
@@ -81,7 +79,6 @@ class ssu_copy_launch_t(ctypes.Structure):
 
 SSU_COPY_AUTO = 0
 SSU_COPY_VEC = 1
-SSU_COPY_BULK = 2
 SSU_COPY_MAX_TENSORS = 64
 
 
@@ -106,6 +103,7 @@ _EXPORTS = {
     "ssu_get_error": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_uint32),
                                      ctypes.POINTER(ctypes.c_int64)]),
     "ssu_set_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_launch_t)]),
+    "ssu_set_launch_override": (ctypes.c_int, [_vp, ctypes.c_char_p]),
     "ssu_get_launch": (ctypes.c_int, [_vp, ctypes.POINTER(ssu_shape_t),
                                       ctypes.POINTER(ssu_launch_t)]),
     "ssu_set_pdl": (ctypes.c_int, [_vp, ctypes.c_int32]),
@@ -128,6 +126,7 @@ _EXPORTS = {
 }
 
 SSU_STATIC_SCRATCH_BYTES = 256
+SSU_ABI_VERSION = 2
 SSU_STATIC_MAX_BATCH = 2147483647
 
 
@@ -143,7 +142,7 @@ def lib() -> ctypes.CDLL:
             fn = getattr(handle, name)
             fn.restype = res
             fn.argtypes = args
-        if handle.ssu_abi_version() != 1:
+        if handle.ssu_abi_version() != SSU_ABI_VERSION:
             raise RuntimeError("libssu.so ABI version mismatch")
         _lib = handle
     return _lib
@@ -295,10 +294,26 @@ def ssu_update_static(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, 
     0xFFFFFFFF, 0].  Calls that overlap on the GPU race on the shared counters.
     """
     shape, strides = describe(state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)
+    if counters_out is not None:
+        _check_counters(counters_out, state_pool)
     ptrs = [_ptr(t) for t in (state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D, out)]
     _check(lib().ssu_update_static(*ptrs, ctypes.byref(shape), ctypes.byref(strides),
                                    _ptr(counters_out), _stream_ptr(stream)),
            "ssu_update_static")
+
+
+def _check_counters(counters_out, state_pool) -> None:
+    """``counters_out`` receives a 12-byte device-to-device copy: it must be a contiguous CUDA
+    tensor of 4-byte elements with at least 3 of them, on the state pool's device."""
+    t = counters_out
+    if not isinstance(t, torch.Tensor):
+        raise ValueError("counters_out must be a torch.Tensor (or None)")
+    if t.device.type != "cuda" or t.device != state_pool.device:
+        raise ValueError(f"counters_out must be on {state_pool.device}, got {t.device}")
+    if t.element_size() != 4 or t.dtype.is_floating_point:
+        raise ValueError(f"counters_out must hold 4-byte integers, got {t.dtype}")
+    if t.numel() < 3 or not t.is_contiguous():
+        raise ValueError("counters_out must be contiguous with at least 3 elements")
 
 
 def ssu_host_workspace_bytes(shape: ssu_shape_t) -> int:
@@ -356,6 +371,13 @@ def ssu_set_launch(handle: int, mode: int = SSU_MODE_AUTO, rows_per_warp: int = 
     """Force a launch shape (mode AUTO restores the built-in table)."""
     cfg = ssu_launch_t(mode, rows_per_warp, warps_per_cta, stages)
     _check(lib().ssu_set_launch(handle, ctypes.byref(cfg)), "ssu_set_launch")
+
+
+def ssu_set_launch_override(handle: int, spec: str | None) -> None:
+    """Force a launch shape from text: "rows_per_warp,warps_per_cta" (optionally "vec,..."),
+    or None / "" / "auto" for the built-in table."""
+    _check(lib().ssu_set_launch_override(handle, None if spec is None else spec.encode()),
+           "ssu_set_launch_override")
 
 
 def ssu_check_indices(state_batch_indices, pool_size: int) -> int:

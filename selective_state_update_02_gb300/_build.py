@@ -14,7 +14,7 @@ CSRC = PKG / "csrc"
 SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_tokens.cu", CSRC / "ssu_copy.cu",
            CSRC / "ssu_host.cpp"]
 HEADERS = [ROOT / "include" / "ssu.h", CSRC / "ssu_device.cuh", CSRC / "ssu_host.h",
-           CSRC / "ssu_vec.cuh", CSRC / "ssu_bulk.cuh", CSRC / "ssu_stage.cuh",
+           CSRC / "ssu_vec.cuh", CSRC / "ssu_stage.cuh",
            CSRC / "ssu_tokens.cuh"]
 OBJDIR = PKG / "_build"
 LIB = PKG / "libssu.so"

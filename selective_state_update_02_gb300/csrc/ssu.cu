@@ -7,24 +7,21 @@
 // reads and writes a 64 x 128 fp32 state (32 KiB each way) and touches ~2.5 KiB of inputs.
 // There is no dense contraction here, so no tensor cores.
 //
-// Two kernels compute it, with the same element mapping and arithmetic (ssu_device.cuh), so
-// every launch shape of either gives bit-identical state and output:
-//   * VEC (ssu_vec.cuh): one CTA per (slab of rows, head, request); each warp holds its rows
-//     in registers, 16-byte vector loads all issued before any use.  The built-in table uses it.
-//   * BULK (ssu_bulk.cuh, fp32 and dstate 128 only): persistent CTAs stream tiles through a
-//     ring of shared-memory stages fed by the TMA engine's 1-D bulk copies; measured slower
-//     than VEC at every size and kept as a forced launch shape.
+// One kernel computes it (ssu_vec.cuh): one CTA per (slab of rows, head, request); each warp
+// holds its rows in registers, 16-byte vector loads all issued before any use.  Every launch
+// shape gives bit-identical state and output (one fixed summation order per row).
 // The multi-token step and the state-block copy live in ssu_tokens.cu and ssu_copy.cu.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cctype>
 #include <climits>
 #include <cstdint>
-#include <mutex>
+#include <cstdlib>
+#include <cstring>
 
 #include "ssu.h"
-#include "ssu_bulk.cuh"
 #include "ssu_device.cuh"
 #include "ssu_stage.cuh"
 #include "ssu_vec.cuh"
@@ -39,19 +36,48 @@ using ssu_host::validate_impl;
 namespace {
 
 
-bool is_pow2_rows(int r, int lo, int hi) {
-    return r >= lo && r <= hi && (r & (r - 1)) == 0;
+// Checks a launch shape by itself (sizes some bucket accepts); rows_per_warp_ok checks it
+// against the call's dstate and state type.
+bool launch_shape_ok(const ssu_launch_t &l) {
+    const int r = l.rows_per_warp;
+    return l.mode == SSU_MODE_VEC && r >= 1 && r <= 32 && (r & (r - 1)) == 0 &&
+           l.warps_per_cta >= 1 && l.warps_per_cta <= kMaxWarpsPerCta;
 }
 
-// Checks a launch shape by itself (sizes the kernels accept).
-bool launch_shape_ok(const ssu_launch_t &l) {
-    if (l.mode == SSU_MODE_VEC)
-        return is_pow2_rows(l.rows_per_warp, 1, 16) && l.warps_per_cta >= 1 &&
-               l.warps_per_cta <= kMaxWarpsPerCta;
-    if (l.mode == SSU_MODE_BULK)
-        return is_pow2_rows(l.rows_per_warp, 2, 16) && l.warps_per_cta >= 1 &&
-               l.warps_per_cta <= kMaxBulkWarps && l.stages >= 2 && l.stages <= kMaxStages;
-    return false;
+// Parses a launch spec: NULL, "", "auto" (the table), or "[vec,]rows_per_warp,warps_per_cta"
+// with optional spaces.  Only the syntax is checked here; ssu_set_launch checks the shape.
+ssu_status_t parse_launch_spec(const char *spec, ssu_launch_t *out) {
+    *out = ssu_launch_t{SSU_MODE_AUTO, 0, 0, 0};
+    if (!spec) return ok();
+    char buf[64];
+    size_t n = 0;
+    for (const char *c = spec; *c; ++c) {
+        if (*c == ' ' || *c == '\t') continue;
+        if (n + 1 >= sizeof(buf)) return fail(SSU_ERR_INVALID_ARG, "launch spec too long");
+        buf[n++] = static_cast<char>(tolower(static_cast<unsigned char>(*c)));
+    }
+    buf[n] = 0;
+    if (n == 0 || strcmp(buf, "auto") == 0) return ok();
+    const char *q = buf;
+    if (strncmp(q, "vec,", 4) == 0) q += 4;
+    int vals[2];
+    for (int i = 0; i < 2; ++i) {
+        if (*q < '0' || *q > '9')
+            return fail(SSU_ERR_INVALID_ARG, "launch spec '%s': expected [vec,]rows,warps", spec);
+        long v = 0;
+        while (*q >= '0' && *q <= '9') {
+            v = v * 10 + (*q++ - '0');
+            if (v > 1024)
+                return fail(SSU_ERR_INVALID_ARG, "launch spec '%s': value too large", spec);
+        }
+        vals[i] = static_cast<int>(v);
+        if (i == 0 && *q++ != ',')
+            return fail(SSU_ERR_INVALID_ARG, "launch spec '%s': expected [vec,]rows,warps", spec);
+    }
+    if (*q)
+        return fail(SSU_ERR_INVALID_ARG, "launch spec '%s': trailing characters", spec);
+    *out = ssu_launch_t{SSU_MODE_VEC, vals[0], vals[1], 0};
+    return ok();
 }
 
 }  // namespace
@@ -60,47 +86,36 @@ namespace {
 
 // Built-in launch-shape table, from the cold-L2 sweeps on GB300 (bench.py --sweep with and
 // without --dstate / --state-dtype, batch 1 to 512, 16 heads, headdim 64), keyed by the bytes
-// of one state row.  A small call gives each warp about 1 KiB of state (2 rows of 512 B, 4 of
-// 256 B; 2 rows at 128 B and 1 KiB) in CTAs of 4 warps; from a size on, 8 rows per warp (4 for
-// 1 KiB rows), in CTAs of 4 warps (2 for a bf16 state of 256 or 512 B rows, and for 1 KiB
-// rows).  The size is counted in state rows per call, for 152 SMs: 4,096 rows of 128 B, 32,768
-// of 256 B, 16,384 of 512 B or 1 KiB (batch 4 / 32 / 16 / 16 at 16 heads of 64 rows).  Against
-// the earlier table (8 rows x 2 warps, stepping down to 4 and 2 rows below 16 warps per SM),
-// e.g. batch 16: fp32 dstate 128 5.02 -> 4.51 us, fp32 dstate 64 3.98 -> 3.30, bf16 dstate 64
-// 4.01 -> 2.78, bf16 dstate 128 4.20 -> 3.42; bf16 dstate 64 at batch 128: 10.41 -> 9.29; fp32
-// dstate 128 at batch 128: 22.25 -> 22.17.  16 rows per warp is slower in every bucket.  The
-// tile never exceeds the headdim.
+// of one state row.  A warp's unit of work is a "slot": the rows one 16-byte vector
+// instruction covers (512 bytes: 1 row of 512 B, 2 of 256 B, 4 of 128 B; a 1 KiB row takes two
+// vectors per lane).  A small call gives each warp 2 slots in CTAs of 4 warps; from a size on,
+// 8 slots per warp (4 rows of 1 KiB), in CTAs of 4 warps (2 for a bf16 state of 512 B rows and
+// for 1 KiB rows).  The size is counted in state bytes per call, for 152 SMs: 8 MiB (batch 16
+// at 16 heads of 64 rows of 512 B; 16 MiB for 1 KiB rows).  16 rows per warp is slower in every bucket.  The tile
+// never exceeds the headdim.
 ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
     (void)st;
     const bool bf16 = s.state_dtype == SSU_STATE_BF16;
     const long long row_bytes = s.dstate * (bf16 ? 2 : 4);
-    const long long rows = s.batch * s.nheads * s.headdim;
-    const long long large_from = row_bytes <= 128 ? 4096 : row_bytes <= 256 ? 32768 : 16384;
-    const bool large = rows * 152 >= large_from * hd.sm_count;
-    int rpw, wpc;
+    const int rpi = ssu_host::rows_per_instruction(s.dstate, s.state_dtype);
+    const long long bytes = s.batch * s.nheads * s.headdim * row_bytes;
+    const long long large_from = row_bytes >= 1024 ? (16LL << 20) : (8LL << 20);
+    const bool large = bytes * 152 >= large_from * hd.sm_count;
+    int slots, wpc;
     if (row_bytes >= 1024) {
-        rpw = large ? 4 : 2;
+        slots = large ? 4 : 2;
         wpc = large ? 2 : 4;
-    } else if (large) {
-        rpw = 8;
-        wpc = bf16 && row_bytes >= 256 ? 2 : 4;
     } else {
-        rpw = row_bytes == 256 ? 4 : 2;
-        wpc = 4;
+        slots = large ? 8 : 2;
+        wpc = large && bf16 && row_bytes >= 512 ? 2 : 4;
     }
-    while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
+    int rpw = slots * rpi;
+    while (slots > 1 && rpw > s.headdim) {
+        slots >>= 1;
+        rpw = slots * rpi;
+    }
     while (wpc > 1 && rpw * wpc > s.headdim) wpc >>= 1;
     return ssu_launch_t{SSU_MODE_VEC, rpw, wpc, 0};
-}
-
-// Whether the BULK kernel can run this call (fp32 state, dstate 128, contiguous rows, and the
-// ring fits in shared memory).
-bool bulk_fits(const ssu_handle_s &hd, const ssu_launch_t &l, const ssu_shape_t &s,
-               const ssu_strides_t *st) {
-    if (s.state_dtype != SSU_STATE_F32 || s.dstate != kDstate) return false;
-    if (st->state[2] != kDstate) return false;
-    const int tile_rows = l.rows_per_warp * l.warps_per_cta;
-    return static_cast<int>(bulk_smem_bytes(l.stages, tile_rows)) <= hd.smem_optin;
 }
 
 // The kernels' parameter block for one call (validated arguments, element strides).
@@ -169,11 +184,6 @@ ssu_status_t ssu_create(ssu_handle_t *out, int32_t device) {
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                    device);
-    for (int rpw = 2; e == cudaSuccess && rpw <= 16; rpw *= 2)
-        for (int i64 = 0; e == cudaSuccess && i64 < 2; ++i64)
-            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(bulk_kernel(rpw, i64 != 0)),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin);
-    if (e == cudaSuccess) e = ssu_host::copy_prepare(h->smem_optin);
     if (e == cudaSuccess) e = cudaMalloc(&h->err, 4 * sizeof(unsigned));
     const unsigned init[4] = {0u, 0xffffffffu, 0u, 0u};
     if (e == cudaSuccess) e = cudaMemcpy(h->err, init, sizeof(init), cudaMemcpyHostToDevice);
@@ -181,6 +191,15 @@ ssu_status_t ssu_create(ssu_handle_t *out, int32_t device) {
         if (h->err) cudaFree(h->err);
         delete h;
         return fail(SSU_ERR_CUDA, "ssu_create: %s", cudaGetErrorString(e));
+    }
+    // SSU_LAUNCH in the environment: the handle's initial launch override.
+    if (const char *env = getenv("SSU_LAUNCH")) {
+        const ssu_status_t st = ssu_set_launch_override(h, env);
+        if (st != SSU_OK) {
+            cudaFree(h->err);
+            delete h;
+            return st;
+        }
     }
     *out = h;
     return ok();
@@ -224,14 +243,17 @@ ssu_status_t ssu_set_launch(ssu_handle_t handle, const ssu_launch_t *launch) {
         return fail(SSU_ERR_UNSUPPORTED,
                     "launch shape mode=%d rows_per_warp=%d warps=%d stages=%d", launch->mode,
                     launch->rows_per_warp, launch->warps_per_cta, launch->stages);
-    if (launch->mode == SSU_MODE_BULK &&
-        static_cast<int>(bulk_smem_bytes(launch->stages,
-                                         launch->rows_per_warp * launch->warps_per_cta)) >
-            handle->smem_optin)
-        return fail(SSU_ERR_UNSUPPORTED, "BULK stages x tile exceed shared memory");
     handle->override_launch = *launch;
     handle->has_override = true;
     return ok();
+}
+
+ssu_status_t ssu_set_launch_override(ssu_handle_t handle, const char *spec) {
+    if (!handle) return fail(SSU_ERR_INVALID_ARG, "NULL handle");
+    ssu_launch_t l{};
+    const ssu_status_t st = parse_launch_spec(spec, &l);
+    if (st != SSU_OK) return st;
+    return ssu_set_launch(handle, l.mode == SSU_MODE_AUTO ? nullptr : &l);
 }
 
 ssu_status_t ssu_set_pdl(ssu_handle_t handle, int32_t enable) {
@@ -252,15 +274,13 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
     const ssu_shape_t &s = *shape;
     ssu_launch_t l = handle->has_override ? handle->override_launch
                                           : table_launch(*handle, s, strides);
-    if (l.mode == SSU_MODE_BULK && !bulk_fits(*handle, l, s, strides)) {
-        if (handle->has_override)
-            return fail(SSU_ERR_UNSUPPORTED,
-                        "BULK mode needs an fp32 state of dstate 128 with contiguous rows");
-        l = ssu_launch_t{SSU_MODE_VEC, 8, 2, 0};
-    }
-    if (l.mode == SSU_MODE_VEC && l.rows_per_warp == 16 &&
-        (s.state_dtype != SSU_STATE_F32 || s.dstate != 128))
-        return fail(SSU_ERR_UNSUPPORTED, "16 rows per warp needs an fp32 state of dstate 128");
+    if (!ssu_host::rows_per_warp_ok(l.rows_per_warp, s.dstate, s.state_dtype))
+        return fail(SSU_ERR_UNSUPPORTED,
+                    "%d rows per warp: dstate %lld with a %s state takes %d x {1, 2, 4, 8}%s",
+                    l.rows_per_warp, (long long)s.dstate,
+                    s.state_dtype == SSU_STATE_BF16 ? "bf16" : "fp32",
+                    ssu_host::rows_per_instruction(s.dstate, s.state_dtype),
+                    s.dstate == 128 && s.state_dtype == SSU_STATE_F32 ? " or 16" : "");
     const int rows_per_tile = l.rows_per_warp * l.warps_per_cta;
     const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
     const long long tiles = s.batch * s.nheads * slabs;
@@ -275,27 +295,11 @@ ssu_status_t ssu_update(ssu_handle_t handle, void *state_pool, const void *state
         return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const bool i64 = s.index_dtype == SSU_INDEX_I64;
-    cudaError_t e;
-    if (l.mode == SSU_MODE_BULK) {
-        const BulkKernel k = bulk_kernel(l.rows_per_warp, i64);
-        const unsigned smem = bulk_smem_bytes(l.stages, rows_per_tile);
-        const int threads = 32 * (1 + l.warps_per_cta);
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
-        if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
-        if (e == cudaSuccess) {
-            const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
-            const unsigned grid = static_cast<unsigned>(tiles < slots ? tiles : slots);
-            const BulkShape q{tiles, l.stages};
-            k<<<grid, threads, smem, cs>>>(p, q);
-            e = cudaGetLastError();
-        }
-    } else {
-        const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
-                        static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
-        e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16, i64,
-                       l.rows_per_warp, l.warps_per_cta, grid, handle->pdl, cs);
-    }
+    const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
+                    static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
+    const cudaError_t e =
+        launch_vec(p, static_cast<int>(s.dstate), s.state_dtype == SSU_STATE_BF16, i64,
+                   l.rows_per_warp, l.warps_per_cta, grid, handle->pdl, cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -314,9 +318,6 @@ ssu_status_t ssu_get_error(ssu_handle_t handle, ssu_stream_t stream, uint32_t *s
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "ssu_get_error: %s", cudaGetErrorString(e));
     if (skipped) *skipped = host[0];
     if (first_bad) *first_bad = host[0] ? static_cast<int64_t>(host[1]) : -1;
-    if (host[2])
-        return fail(SSU_ERR_TIMEOUT, "%u pipeline wait(s) timed out; results are incomplete",
-                    host[2]);
     if (host[0]) return fail(SSU_ERR_INDEX_OOB, "%u request(s) named a slot outside the pool",
                              host[0]);
     return ok();
@@ -415,8 +416,9 @@ ssu_status_t ssu_update_from_host(ssu_handle_t handle, void *state_pool,
     ssu_launch_t l = handle->has_override && handle->override_launch.mode == SSU_MODE_VEC
                          ? handle->override_launch
                          : table_launch(*handle, s, strides);
-    if (l.rows_per_warp == 16 && (s.state_dtype != SSU_STATE_F32 || s.dstate != 128))
-        return fail(SSU_ERR_UNSUPPORTED, "16 rows per warp needs an fp32 state of dstate 128");
+    if (!ssu_host::rows_per_warp_ok(l.rows_per_warp, s.dstate, s.state_dtype))
+        return fail(SSU_ERR_UNSUPPORTED, "%d rows per warp do not fit dstate %lld",
+                    l.rows_per_warp, (long long)s.dstate);
     const int rows_per_tile = l.rows_per_warp * l.warps_per_cta;
     const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
     const long long tiles = s.batch * s.nheads * slabs;
@@ -472,7 +474,7 @@ ssu_status_t ssu_update_from_host(ssu_handle_t handle, void *state_pool,
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_stage(q, handle->sm_count, handle->pdl, cs);
     if (e == cudaSuccess)
-        e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16,
+        e = launch_vec(p, static_cast<int>(s.dstate), s.state_dtype == SSU_STATE_BF16,
                        s.index_dtype == SSU_INDEX_I64, l.rows_per_warp, l.warps_per_cta,
                        dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
                             static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535)),
@@ -491,31 +493,21 @@ static __device__ __align__(256) unsigned ssu_static_scratch[SSU_STATIC_SCRATCH_
 
 namespace {
 
-constexpr int kStaticMaxDevices = 64;
-std::mutex g_static_mutex;
-unsigned *g_static_addr[kStaticMaxDevices] = {};
-int g_static_sms[kStaticMaxDevices] = {};
-
-// Device address of the array on the current device `dev`, looked up once per device.
+// Device address of the array and the SM count of the current device `dev`.  Looked up on
+// every call rather than cached: the address belongs to the device's current context, which
+// a device reset replaces (the lookup is a host-side table read once the library's module is
+// loaded on the device; the first call on a device loads it).
 ssu_status_t static_scratch_on(int dev, unsigned **addr, int *sms) {
-    if (dev < 0 || dev >= kStaticMaxDevices)
-        return fail(SSU_ERR_UNSUPPORTED, "device %d is beyond the %d devices supported", dev,
-                    kStaticMaxDevices);
-    std::lock_guard<std::mutex> lock(g_static_mutex);
-    if (!g_static_addr[dev]) {
-        void *ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, ssu_static_scratch);
-        if (e != cudaSuccess)
-            return fail(SSU_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        int n = 0;
-        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess)
-            return fail(SSU_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
-        g_static_sms[dev] = n;
-        g_static_addr[dev] = static_cast<unsigned *>(ptr);
-    }
-    *addr = g_static_addr[dev];
-    *sms = g_static_sms[dev];
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, ssu_static_scratch);
+    if (e != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return fail(SSU_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    *addr = static_cast<unsigned *>(ptr);
+    *sms = n;
     return SSU_OK;
 }
 
@@ -550,7 +542,6 @@ extern "C" ssu_status_t ssu_update_static(void *state_pool, const void *state_ba
     ssu_handle_s table_only;
     table_only.sm_count = sms;
     ssu_launch_t l = table_launch(table_only, s, strides);
-    if (l.mode != SSU_MODE_VEC) l = ssu_launch_t{SSU_MODE_VEC, 8, 2, 0};
     const int rows_per_tile = l.rows_per_warp * l.warps_per_cta;
     const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
     const long long tiles = s.batch * s.nheads * slabs;
@@ -560,11 +551,11 @@ extern "C" ssu_status_t ssu_update_static(void *state_pool, const void *state_ba
                                     out, s, strides, slabs, rows_per_tile, scratch);
 
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    // The counters start every call at {0 skipped, no smallest index (all ones), 0 timeouts}.
+    // The counters start every call at {0 skipped, no smallest index (all ones), 0 (reserved)}.
     e = cudaMemsetAsync(scratch, 0, 3 * sizeof(unsigned), cs);
     if (e == cudaSuccess) e = cudaMemsetAsync(scratch + 1, 0xff, sizeof(unsigned), cs);
     if (e == cudaSuccess)
-        e = launch_vec(p, static_cast<int>(s.dstate / 32), s.state_dtype == SSU_STATE_BF16,
+        e = launch_vec(p, static_cast<int>(s.dstate), s.state_dtype == SSU_STATE_BF16,
                        s.index_dtype == SSU_INDEX_I64, l.rows_per_warp, l.warps_per_cta,
                        dim3(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
                             static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535)),

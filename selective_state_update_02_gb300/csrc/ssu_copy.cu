@@ -7,11 +7,9 @@
 // chunks of tensor t occupy a contiguous range of a global chunk index (tensor-major, then
 // request, then chunk), so the whole call is one flat list that persistent CTAs stride through.
 //
-// VEC: each thread moves `vectors` 16-byte words per pass, all loads issued before the stores.
-// BULK: one thread per CTA drives the TMA engine: 1-D `cp.async.bulk` loads of whole chunks
-// into a ring of shared-memory stages (completion on the stage's mbarrier), each followed by a
-// 1-D bulk store of the stage to its destination; a stage is reused once the store issued from
-// it has been read out (`cp.async.bulk.wait_group.read`).  Every mbarrier wait is bounded.
+// Each thread moves `vectors` 16-byte words per pass, all loads issued before the stores.
+// (A variant driving the TMA engine's 1-D bulk copies through a shared-memory ring was measured
+// slower at every size and is not part of the library.)
 
 #include <cuda_runtime.h>
 
@@ -47,7 +45,7 @@ struct CopyParams {
     long long chunk_bytes;
     int num_tensors;
     int idx64;
-    unsigned *err;  // [0] skipped requests, [1] smallest skipped request, [2] timeouts
+    unsigned *err;  // [0] skipped requests, [1] smallest skipped request
 };
 
 struct ChunkRef {
@@ -117,83 +115,6 @@ __global__ void __launch_bounds__(256) copy_vec_kernel(const __grid_constant__ C
     pdl_trigger();
 }
 
-__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, unsigned bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_u32(src_smem)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until at most N committed bulk-store groups may still be reading shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// One thread per CTA (threadIdx.x == 0) drives the ring; `stages` is at most kMaxStages.
-// Loads run L = stages - 2 chunks ahead of the stores, so a stage is refilled once the store
-// issued two iterations earlier has been read out (wait_group.read 1).
-__global__ void __launch_bounds__(32) copy_bulk_kernel(const __grid_constant__ CopyParams p,
-                                                       int stages) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    if (threadIdx.x != 0) return;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw);
-    unsigned char *buf = smem_raw + 128;
-    const unsigned chunk = static_cast<unsigned>(p.chunk_bytes);
-    const long long G = gridDim.x;
-    const long long n_my = (p.total_chunks - blockIdx.x + G - 1) / G;
-    const int L = stages - 2;
-    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
-    fence_mbarrier_init();
-
-    unsigned valid_bits = 0;  // bit s: the chunk loaded into stage s is to be stored
-    ChunkRef ref[kMaxStages];
-    bool failed = false;
-    long long issued = 0;
-    for (long long j = 0; j < n_my + L; ++j) {
-        if (j < n_my) {  // load chunk j into stage j % stages
-            const int st = static_cast<int>(j % stages);
-            if (j >= stages) bulk_wait_read<1>();
-            const ChunkRef r = locate_chunk(p, blockIdx.x + j * G);
-            ref[st] = r;
-            if (r.valid) {
-                valid_bits |= 1u << st;
-                mbar_arrive_expect_tx(&full[st], r.bytes);
-                bulk_load(buf + static_cast<size_t>(st) * chunk, r.src, r.bytes, &full[st]);
-            } else {
-                valid_bits &= ~(1u << st);
-                mbar_arrive(&full[st]);
-            }
-            issued = j + 1;
-        }
-        const long long m = j - L;  // store chunk m
-        if (m >= 0 && m < n_my) {
-            const int st = static_cast<int>(m % stages);
-            if (!mbar_wait(&full[st], static_cast<unsigned>((m / stages) & 1))) {
-                failed = true;
-                break;
-            }
-            if (valid_bits & (1u << st))
-                bulk_store(ref[st].dst, buf + static_cast<size_t>(st) * chunk, ref[st].bytes);
-            bulk_commit();  // one group per iteration (empty for a skipped chunk), so the
-                            // wait_group.read count above always names the right store
-        }
-    }
-    bulk_wait_all();
-    if (failed) {
-        atomicAdd(&p.err[2], 1u);
-        for (long long j = issued > stages ? issued - stages : 0; j < issued; ++j)
-            mbar_wait(&full[j % stages], static_cast<unsigned>((j / stages) & 1));
-    }
-}
-
 template <int V>
 cudaError_t launch_copy_vec_one(const CopyParams &p, int threads, unsigned grid, bool pdl,
                                 cudaStream_t st) {
@@ -240,7 +161,6 @@ bool copy_launch_ok(const ssu_copy_launch_t &l) {
     if (l.mode == SSU_COPY_VEC)
         return vec_copy_kernel(l.stages) != nullptr && l.threads >= 32 && l.threads <= 256 &&
                l.threads % 32 == 0;
-    if (l.mode == SSU_COPY_BULK) return l.stages >= 3 && l.stages <= kMaxStages;
     return false;
 }
 
@@ -254,15 +174,6 @@ ssu_copy_launch_t copy_table(long long total_bytes) {
 
 }  // namespace
 
-namespace ssu_host {
-
-cudaError_t copy_prepare(int smem_optin) {
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(copy_bulk_kernel),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
-}
-
-}  // namespace ssu_host
-
 extern "C" {
 
 ssu_status_t ssu_copy_set_launch(ssu_handle_t handle, const ssu_copy_launch_t *launch) {
@@ -274,9 +185,6 @@ ssu_status_t ssu_copy_set_launch(ssu_handle_t handle, const ssu_copy_launch_t *l
     if (!copy_launch_ok(*launch))
         return fail(SSU_ERR_UNSUPPORTED, "copy launch mode=%d chunk_kib=%d stages=%d threads=%d",
                     launch->mode, launch->chunk_kib, launch->stages, launch->threads);
-    if (launch->mode == SSU_COPY_BULK &&
-        128 + launch->stages * launch->chunk_kib * 1024 > handle->smem_optin)
-        return fail(SSU_ERR_UNSUPPORTED, "BULK copy stages x chunk exceed shared memory");
     handle->copy_override = *launch;
     handle->has_copy_override = true;
     return ok();
@@ -341,25 +249,13 @@ ssu_status_t ssu_copy_blocks(ssu_handle_t handle, const ssu_block_tensor_t *tens
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     int per_sm = 0;
-    if (l.mode == SSU_COPY_BULK) {
-        const int smem = 128 + l.stages * l.chunk_kib * 1024;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, copy_bulk_kernel, 32, smem);
-        if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
-        if (e == cudaSuccess) {
-            const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
-            const unsigned grid = static_cast<unsigned>(chunks < slots ? chunks : slots);
-            copy_bulk_kernel<<<grid, 32, smem, cs>>>(p, l.stages);
-            e = cudaGetLastError();
-        }
-    } else {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vec_copy_kernel(l.stages),
-                                                          l.threads, 0);
-        if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
-        if (e == cudaSuccess) {
-            const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
-            const unsigned grid = static_cast<unsigned>(chunks < slots ? chunks : slots);
-            e = launch_copy_vec(p, l.stages, l.threads, grid, handle->pdl, cs);
-        }
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vec_copy_kernel(l.stages),
+                                                      l.threads, 0);
+    if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
+    if (e == cudaSuccess) {
+        const long long slots = static_cast<long long>(per_sm) * handle->sm_count;
+        const unsigned grid = static_cast<unsigned>(chunks < slots ? chunks : slots);
+        e = launch_copy_vec(p, l.stages, l.threads, grid, handle->pdl, cs);
     }
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "copy launch: %s", cudaGetErrorString(e));
     return ok();

@@ -1,6 +1,6 @@
 // Device-side pieces shared by the decode-step kernels: launch constants, the parameter block,
-// the per-element arithmetic, the readout reduction, slot lookup, and the mbarrier / bulk-copy
-// PTX wrappers.  Included by each kernel translation unit (internal linkage per unit).
+// the per-element arithmetic, the readout reduction, slot lookup and programmatic dependent
+// launch.  Included by each kernel translation unit (internal linkage per unit).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -10,12 +10,7 @@
 
 namespace {
 
-constexpr int kDstate = 128;             // dstate of the BULK kernel: 32 lanes x 4 columns
-constexpr int kRowBytes = kDstate * 4;   // one fp32 state row of the BULK kernel
-constexpr int kMaxWarpsPerCta = 16;      // VEC
-constexpr int kMaxBulkWarps = 8;         // BULK compute warps (plus one producer warp)
-constexpr int kMaxStages = 8;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per mbarrier wait
+constexpr int kMaxWarpsPerCta = 16;
 
 // Everything one launch needs, passed by value in the kernel parameter space.
 struct SsuParams {
@@ -39,13 +34,7 @@ struct SsuParams {
     unsigned long long group_magic;  // group_magic(heads_per_group): see group_of
     int slabs;         // tiles per (request, head) unit
     int rows_per_cta;  // rows per tile
-    unsigned *err;     // [0] skipped requests, [1] smallest skipped request, [2] timeouts
-};
-
-// BULK launch geometry.
-struct BulkShape {
-    long long tiles;  // batch * nheads * slabs
-    int stages;
+    unsigned *err;     // [0] skipped requests, [1] smallest skipped request
 };
 
 // Group of head h, floor(h / d) for d = heads per group, without an integer division (the
@@ -61,41 +50,97 @@ __host__ __device__ __forceinline__ int group_of(int h, unsigned long long m) {
     return static_cast<int>((static_cast<unsigned long long>(h) * m) >> 32);
 }
 
+// floor(n / d) for 0 <= n < 2^31 and 1 <= d < 2^31 by a multiply and a shift.  With
+// l = ceil(log2 d) and m = floor(2^(31+l) / d) + 1:  2^(31+l) < m d <= 2^(31+l) + d <=
+// 2^(31+l) + 2^l, and for such m, floor(n m / 2^(31+l)) = floor(n / d) for every n < 2^31
+// (Granlund and Montgomery, "Division by invariant integers using multiplication", 1994,
+// Theorem 4.2 with N = 31).  m <= 2^32 + 1, so n m < 2^64 needs no wider product.
+struct FastDiv {
+    unsigned long long m;
+    unsigned shift;
+};
+
+__host__ __device__ inline FastDiv fast_div(unsigned d) {
+    unsigned l = 0;
+    while ((1ull << l) < d) ++l;
+    return FastDiv{(1ull << (31 + l)) / d + 1, 31 + l};
+}
+
+__host__ __device__ __forceinline__ unsigned fast_div_apply(unsigned n, FastDiv f) {
+    return static_cast<unsigned>((static_cast<unsigned long long>(n) * f.m) >> f.shift);
+}
+
 __device__ __forceinline__ float softplus_f32(float z) {
     // log(1 + e^z); above 20 the correction is below fp32 resolution of z.
     return z > 20.0f ? z : log1pf(expf(z));
 }
 
-// The update of one lane's 4 columns of one row; returns the lane's part of the readout.
-__device__ __forceinline__ float update_cols(float4 &w, float dA, float k, const float (&bb)[4],
-                                             const float (&cc)[4]) {
-    w.x = fmaf(w.x, dA, k * bb[0]);
-    w.y = fmaf(w.y, dA, k * bb[1]);
-    w.z = fmaf(w.z, dA, k * bb[2]);
-    w.w = fmaf(w.w, dA, k * bb[3]);
-    float part = w.x * cc[0];
-    part = fmaf(w.y, cc[1], part);
-    part = fmaf(w.z, cc[2], part);
-    part = fmaf(w.w, cc[3], part);
-    return part;
-}
-
 // ---------------------------------------------------------------------------------------
-// Columns of a row owned by one lane, for dstate N = 32 * NC (NC = 2, 4 or 8).  With NC = 2
-// lane l owns columns 2l, 2l+1; with NC = 4 columns 4l..4l+3; with NC = 8 the two groups
-// 4l..4l+3 and 128+4l..128+4l+3, so every vector instruction of a warp covers one contiguous
-// span of the row.  The lane's j-th value is column lane_offset<NC>(lane) + (j / 4) * 128 +
-// j % 4.
+// Lane geometry of a state row.  A row of dstate N elements of type ST (N * sizeof(ST) bytes)
+// is read with 16-byte vectors.  A row of 512 bytes or more spreads over all 32 lanes, each
+// lane holding VPR = bytes / 512 vectors (column groups L * EPV apart).  A shorter row (256 or
+// 128 bytes) spreads over L = 16 or 8 lanes, so one warp-wide vector instruction covers
+// RPI = 32 / L consecutive rows: lane l works on row-in-instruction l / L, column group l % L.
+// Every warp-wide load or store thus moves 512 contiguous bytes of a contiguous state, and the
+// per-warp work (slot lookup, scalars, addresses, the readout tree's shuffles) is spread over
+// 512 bytes per instruction whatever the row size.
+//
+//   dstate, state   row bytes   L    RPI   columns per lane (NC)
+//   64, fp32        256         16   2     4
+//   128, fp32       512         32   1     4
+//   256, fp32       1024        32   1     8  (4 + 4, 128 apart)
+//   64, bf16        128         8    4     8
+//   128, bf16       256         16   2     8
+//   256, bf16       512         32   1     8
+//
+// A lane's e-th value is column (e / EPV) * L * EPV + (l % L) * EPV + e % EPV.  A "slot" is
+// what one vector instruction of a warp covers: RPI rows.  The readout of a row sums the
+// lane's NC products in order e = 0, 1, ... and then the L lanes of the row by the xor tree
+// L/2, ..., 2, 1 (reduce_rows); every kernel and launch shape uses that order, so all give
+// the same bits.
+template <int N, typename ST>
+struct RowGeo {
+    static constexpr int kEPV = 16 / static_cast<int>(sizeof(ST));  // elements per vector
+    static constexpr int kRowBytes = N * static_cast<int>(sizeof(ST));
+    static constexpr int L = kRowBytes >= 512 ? 32 : kRowBytes / 16;
+    static constexpr int RPI = 32 / L;
+    static constexpr int VPR = kRowBytes >= 512 ? kRowBytes / 512 : 1;
+    static constexpr int NC = VPR * kEPV;
+    static constexpr int kVecStride = L * kEPV;  // columns between a lane's vectors
+    static_assert(kRowBytes >= 128 && kRowBytes <= 1024, "dstate 64, 128 or 256");
+};
 
-// Offset of a lane's first column in a row (its columns then sit at +0..3 and, for NC = 8,
-// +128..131; for NC = 2 at +0..1).  Kernels add it to the row pointer once.
-template <int NC>
-__device__ __forceinline__ int lane_offset(int lane) {
-    return NC == 2 ? 2 * lane : 4 * lane;
+// Offset (elements) of the lane's first column within its row.
+template <class G>
+__device__ __forceinline__ int col0_of(int lane) {
+    return G::L == 32 ? lane * G::kEPV : (lane & (G::L - 1)) * G::kEPV;
 }
 
-__device__ __forceinline__ float2 bf2_to_f2(unsigned bits) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bits));
+// Row of the lane within one vector instruction (0 .. RPI - 1).
+template <class G>
+__device__ __forceinline__ int sub_of(int lane) {
+    return G::RPI == 1 ? 0 : lane / G::L;
+}
+
+// A lane's share of one row as loaded: VPR 16-byte vectors.
+template <class G>
+struct RawRow {
+    uint4 w[G::VPR];
+};
+
+// Streaming (evict-first) load of the lane's vectors of a row; `p` points at its first column.
+template <class G, typename ST>
+__device__ __forceinline__ void load_raw(const ST *p, RawRow<G> &r) {
+#pragma unroll
+    for (int v = 0; v < G::VPR; ++v)
+        r.w[v] = __ldcs(reinterpret_cast<const uint4 *>(p + v * G::kVecStride));
+}
+
+template <class G, typename ST>
+__device__ __forceinline__ void store_raw(ST *p, const RawRow<G> &r) {
+#pragma unroll
+    for (int v = 0; v < G::VPR; ++v)
+        __stcs(reinterpret_cast<uint4 *>(p + v * G::kVecStride), r.w[v]);
 }
 
 __device__ __forceinline__ unsigned f2_to_bf2(float a, float b) {
@@ -103,74 +148,97 @@ __device__ __forceinline__ unsigned f2_to_bf2(float a, float b) {
     return *reinterpret_cast<const unsigned *>(&h);
 }
 
-// Streaming (evict-first) load of one lane's NC columns of a row, widened to fp32.  `p` points
-// at the lane's first column (row + lane_offset<NC>(lane)).
-template <int NC, typename ST>
-__device__ __forceinline__ void load_cols(const ST *p, float (&v)[NC]) {
-    if constexpr (sizeof(ST) == 4) {
-        if constexpr (NC == 2) {
-            const float2 a = __ldcs(reinterpret_cast<const float2 *>(p));
-            v[0] = a.x, v[1] = a.y;
-        } else {
+// The lane's NC values of a row as fp32 (bf16 widens exactly: it is the top half of an fp32).
+template <class G, typename ST>
+__device__ __forceinline__ void raw_to_f32(const RawRow<G> &r, float (&v)[G::NC]) {
 #pragma unroll
-            for (int g = 0; g < NC / 4; ++g) {
-                const float4 a = __ldcs(reinterpret_cast<const float4 *>(p + g * 128));
-                v[4 * g] = a.x, v[4 * g + 1] = a.y, v[4 * g + 2] = a.z, v[4 * g + 3] = a.w;
-            }
-        }
-    } else {
-        if constexpr (NC == 2) {
-            const float2 a = bf2_to_f2(__ldcs(reinterpret_cast<const unsigned *>(p)));
-            v[0] = a.x, v[1] = a.y;
-        } else {
+    for (int q = 0; q < G::VPR; ++q) {
+        const unsigned w[4] = {r.w[q].x, r.w[q].y, r.w[q].z, r.w[q].w};
 #pragma unroll
-            for (int g = 0; g < NC / 4; ++g) {
-                const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p + g * 128));
-                const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y);
-                v[4 * g] = a.x, v[4 * g + 1] = a.y, v[4 * g + 2] = b.x, v[4 * g + 3] = b.y;
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (sizeof(ST) == 4) {
+                v[4 * q + i] = __uint_as_float(w[i]);
+            } else {
+                v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+                v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
             }
         }
     }
 }
 
-// Streaming store of one lane's NC columns (rounded to bf16, nearest even, for a bf16 state);
-// `p` points at the lane's first column.
-template <int NC, typename ST>
-__device__ __forceinline__ void store_cols(ST *p, const float (&v)[NC]) {
-    if constexpr (sizeof(ST) == 4) {
-        if constexpr (NC == 2) {
-            __stcs(reinterpret_cast<float2 *>(p), make_float2(v[0], v[1]));
-        } else {
+// The values back in the state's format (a bf16 state rounds to nearest even).
+template <class G, typename ST>
+__device__ __forceinline__ void f32_to_raw(const float (&v)[G::NC], RawRow<G> &r) {
 #pragma unroll
-            for (int g = 0; g < NC / 4; ++g)
-                __stcs(reinterpret_cast<float4 *>(p + g * 128),
-                       make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]));
-        }
-    } else {
-        if constexpr (NC == 2) {
-            __stcs(reinterpret_cast<unsigned *>(p), f2_to_bf2(v[0], v[1]));
-        } else {
+    for (int q = 0; q < G::VPR; ++q) {
+        unsigned w[4];
 #pragma unroll
-            for (int g = 0; g < NC / 4; ++g)
-                __stcs(reinterpret_cast<uint2 *>(p + g * 128),
-                       make_uint2(f2_to_bf2(v[4 * g], v[4 * g + 1]),
-                                  f2_to_bf2(v[4 * g + 2], v[4 * g + 3])));
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (sizeof(ST) == 4)
+                w[i] = __float_as_uint(v[4 * q + i]);
+            else
+                w[i] = f2_to_bf2(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
         }
+        r.w[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
-// The lane's NC columns of B (or C), widened to fp32; `p` points at the lane's first column.
-template <int NC>
-__device__ __forceinline__ void load_bc(const __nv_bfloat16 *p, float (&o)[NC]) {
+// The lane's NC columns of B (or C) widened to fp32; `p` points at its first column.  With
+// `vec` (the warp found the row's address aligned to a whole column group: 2 * EPV bytes), one
+// load per group; otherwise element by element.
+template <class G>
+__device__ __forceinline__ void load_bc(const __nv_bfloat16 *p, bool vec, float (&o)[G::NC]) {
+    const unsigned short *q = reinterpret_cast<const unsigned short *>(p);
+    if (vec) {
 #pragma unroll
-    for (int j = 0; j < NC; ++j) o[j] = __bfloat162float(p[(j / 4) * 128 + (j % 4)]);
+        for (int v = 0; v < G::VPR; ++v) {
+            unsigned w[G::kEPV / 2];
+            if constexpr (G::kEPV == 8) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(q + v * G::kVecStride);
+                w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+            } else {
+                const uint2 u = *reinterpret_cast<const uint2 *>(q + v * G::kVecStride);
+                w[0] = u.x, w[1] = u.y;
+            }
+#pragma unroll
+            for (int i = 0; i < G::kEPV / 2; ++i) {
+                o[v * G::kEPV + 2 * i] = __uint_as_float(w[i] << 16);
+                o[v * G::kEPV + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < G::NC; ++e)
+            o[e] = __uint_as_float(
+                static_cast<unsigned>(q[(e / G::kEPV) * G::kVecStride + e % G::kEPV]) << 16);
+    }
 }
 
-// The update of one lane's NC columns of one row; returns the lane's part of the readout
-// (its columns summed in order j = 0, 1, ...); for NC = 4 the same operations as update_cols.
+// The update of the lane's NC values of one row, S' = S dA + k B (k = dt x of the row), in
+// packed fp32x2 instructions (IEEE round to nearest per element: the values of fmaf(S, dA,
+// k * B)); returns the lane's part of the readout, its products S' C summed in order.
 template <int NC>
 __device__ __forceinline__ float update_lane(float (&v)[NC], float dA, float k,
                                              const float (&bb)[NC], const float (&cc)[NC]) {
+    const float2 k2 = make_float2(k, k), dA2 = make_float2(dA, dA);
+#pragma unroll
+    for (int i = 0; i < NC / 2; ++i) {
+        const float2 w = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), dA2,
+                                    __fmul2_rn(k2, make_float2(bb[2 * i], bb[2 * i + 1])));
+        v[2 * i] = w.x;
+        v[2 * i + 1] = w.y;
+    }
+    float part = v[0] * cc[0];
+#pragma unroll
+    for (int j = 1; j < NC; ++j) part = fmaf(v[j], cc[j], part);
+    return part;
+}
+
+// The same values by scalar instructions (fmaf(S, dA, k * B) per element).
+template <int NC>
+__device__ __forceinline__ float update_lane_scalar(float (&v)[NC], float dA, float k,
+                                                    const float (&bb)[NC],
+                                                    const float (&cc)[NC]) {
 #pragma unroll
     for (int j = 0; j < NC; ++j) v[j] = fmaf(v[j], dA, k * bb[j]);
     float part = v[0] * cc[0];
@@ -179,17 +247,18 @@ __device__ __forceinline__ float update_lane(float (&v)[NC], float dA, float k,
     return part;
 }
 
-// Sums R per-lane parts (one per row) over the 32 lanes.  The pairs are always formed by xor
-// masks 16, 8, 4, 2, 1 in that order (the tree of a plain butterfly), but while a lane holds
-// more than one row it hands half of its rows to its partner at each step ("reduce-scatter"),
-// which needs R - 1 + (5 - log2 R) shuffles instead of 5 R.  Each sum is the same IEEE value the
+// Sums R per-lane parts (one per slot) over the L lanes of each row.  The pairs are always
+// formed by xor masks L/2, ..., 2, 1 in that order (the tree of a plain butterfly over the row's
+// lanes; masks below L never leave the row's group of lanes), but while a lane holds more than
+// one slot it hands half of them to its partner at each step ("reduce-scatter"), which needs
+// R - 1 + (log2 L - log2 R) shuffles instead of R log2 L.  Each sum is the same IEEE value the
 // plain butterfly gives (a + b == b + a exactly), whatever R is.  Afterwards lane l holds the
-// total of row row_of_lane<R>(l).
-template <int R>
+// total of slot slot_of_lane<R, L>(l) of its row group.
+template <int R, int L>
 __device__ __forceinline__ float reduce_rows(float (&v)[R], int lane) {
-    static_assert(R >= 1 && R <= 32 && (R & (R - 1)) == 0, "R must be a power of two <= 32");
+    static_assert(R >= 1 && R <= L && (R & (R - 1)) == 0, "R must be a power of two <= L");
 #pragma unroll
-    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1) {
+    for (int n = R, m = L / 2; n > 1; n >>= 1, m >>= 1) {
         const bool upper = (lane & m) != 0;
 #pragma unroll
         for (int j = 0; j < n / 2; ++j) {
@@ -200,24 +269,24 @@ __device__ __forceinline__ float reduce_rows(float (&v)[R], int lane) {
     }
     float t = v[0];
 #pragma unroll
-    for (int m = 16 / R; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+    for (int m = L / (2 * R); m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
     return t;
 }
 
-// The row whose total lane l holds after reduce_rows<R>.
-template <int R>
-__device__ __forceinline__ int row_of_lane(int lane) {
-    int row = 0;
+// The slot whose total lane l holds after reduce_rows<R, L>.
+template <int R, int L>
+__device__ __forceinline__ int slot_of_lane(int lane) {
+    int slot = 0;
 #pragma unroll
-    for (int n = R, m = 16; n > 1; n >>= 1, m >>= 1)
-        if (lane & m) row += n / 2;
-    return row;
+    for (int n = R, m = L / 2; n > 1; n >>= 1, m >>= 1)
+        if (lane & m) slot += n / 2;
+    return slot;
 }
 
-// Lanes that write a readout: one per group of lanes holding the same row.
-template <int R>
+// Lanes that write a readout: one per group of lanes holding the same slot's total.
+template <int R, int L>
 __device__ __forceinline__ bool writes_row(int lane) {
-    return (lane & (32 / R - 1)) == 0;
+    return (lane & (L / R - 1)) == 0;
 }
 
 // Programmatic dependent launch.  pdl_wait blocks until the grid this one depends on has
@@ -241,70 +310,6 @@ __device__ __forceinline__ long long load_slot(const SsuParams &p, long long b) 
 __device__ __forceinline__ void record_skip(const SsuParams &p, long long b) {
     atomicAdd(&p.err[0], 1u);
     atomicMin(&p.err[1], static_cast<unsigned>(b));
-}
-
-// ---------------------------------------------------------------------------------------
-// BULK kernel: PTX helpers (mbarrier, bulk asynchronous copies, proxy fence)
-
-__device__ __forceinline__ unsigned smem_u32(const void *ptr) {
-    return static_cast<unsigned>(__cvta_generic_to_shared(ptr));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
-    unsigned done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase of `parity` to complete; false after kWaitLimitNs without completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-#pragma unroll 1
-        for (int k = 0; k < 32; ++k)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, unsigned bytes,
-                                          uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_mbarrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
 }  // namespace

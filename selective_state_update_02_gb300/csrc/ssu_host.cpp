@@ -98,6 +98,19 @@ ssu_status_t validate_impl(const void *state_pool, const void *idx, const uint16
     return ok();
 }
 
+int rows_per_instruction(int64_t dstate, int32_t state_dtype) {
+    const int64_t row_bytes = dstate * (state_dtype == SSU_STATE_BF16 ? 2 : 4);
+    return row_bytes >= 512 ? 1 : static_cast<int>(512 / row_bytes);
+}
+
+bool rows_per_warp_ok(int rows_per_warp, int64_t dstate, int32_t state_dtype) {
+    if (dstate == 128 && state_dtype == SSU_STATE_F32 && rows_per_warp == 16) return true;
+    const int rpi = rows_per_instruction(dstate, state_dtype);
+    for (int slots = 1; slots <= 8; slots *= 2)
+        if (rows_per_warp == slots * rpi) return true;
+    return false;
+}
+
 }  // namespace ssu_host
 
 extern "C" {
@@ -112,7 +125,6 @@ const char *ssu_status_string(ssu_status_t status) {
         case SSU_ERR_MISALIGNED: return "SSU_ERR_MISALIGNED";
         case SSU_ERR_CUDA: return "SSU_ERR_CUDA";
         case SSU_ERR_INDEX_OOB: return "SSU_ERR_INDEX_OOB";
-        case SSU_ERR_TIMEOUT: return "SSU_ERR_TIMEOUT";
     }
     return "SSU_ERR_UNKNOWN";
 }

@@ -22,9 +22,12 @@ ssu_status_t validate_impl(const void *state_pool, const void *idx, const uint16
                            const uint16_t *out, const ssu_shape_t *shape,
                            const ssu_strides_t *st);
 
-// Lets the BULK block-copy kernel use up to `smem_optin` bytes of dynamic shared memory
-// (called once per handle by ssu_create, on the handle's device).
-cudaError_t copy_prepare(int smem_optin);
+// Rows one warp-wide 16-byte vector instruction covers for this dstate and state type: 1 for
+// rows of 512 bytes or more, 2 for 256-byte rows, 4 for 128-byte rows (the kernels' RowGeo).
+int rows_per_instruction(int64_t dstate, int32_t state_dtype);
+// Whether a kernel instantiation exists for `rows_per_warp` rows per warp: rows_per_instruction
+// x {1, 2, 4, 8}, and 16 for an fp32 state of dstate 128.
+bool rows_per_warp_ok(int rows_per_warp, int64_t dstate, int32_t state_dtype);
 
 // Restores the caller's current device on scope exit.
 struct DeviceGuard {
@@ -49,7 +52,7 @@ struct ssu_handle_s {
     int device = 0;
     int sm_count = 0;
     int smem_optin = 0;       // max dynamic shared memory per CTA (bytes)
-    unsigned *err = nullptr;  // device: [0] skipped, [1] smallest skipped request, [2] timeouts
+    unsigned *err = nullptr;  // device: [0] skipped, [1] smallest skipped request, [2] 0
     bool has_override = false;
     ssu_launch_t override_launch{};
     bool has_copy_override = false;

@@ -17,6 +17,43 @@ using ssu_host::fail;
 using ssu_host::ok;
 using ssu_host::validate_impl;
 
+namespace {
+
+template <int N, typename ST, bool kIdx64>
+cudaError_t launch_tokens_t(const TokenParams &q, dim3 grid, int rpw, int warps, bool pdl,
+                            cudaStream_t st) {
+    constexpr int RPI = RowGeo<N, ST>::RPI;
+    constexpr int PD = token_prefetch<N, ST>();
+#define SSU_TOK(R_) launch_tokens_one<R_, N, ST, kIdx64, PD>(q, grid, warps, pdl, st)
+    if (rpw == RPI) return SSU_TOK(RPI);
+    if (rpw == 2 * RPI) return SSU_TOK(2 * RPI);
+    if (rpw == 4 * RPI) return SSU_TOK(4 * RPI);
+    if (rpw == 8 * RPI) return SSU_TOK(8 * RPI);
+    if constexpr (N == 128 && sizeof(ST) == 4)
+        if (rpw == 16) return SSU_TOK(16);
+#undef SSU_TOK
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tokens(const TokenParams &q, dim3 grid, int dstate, bool bf16, bool i64,
+                          int rpw, int warps, bool pdl, cudaStream_t st) {
+#define SSU_TOK_N(N_)                                                                         \
+    if (dstate == N_) {                                                                       \
+        if (bf16)                                                                             \
+            return i64 ? launch_tokens_t<N_, __nv_bfloat16, true>(q, grid, rpw, warps, pdl, st) \
+                       : launch_tokens_t<N_, __nv_bfloat16, false>(q, grid, rpw, warps, pdl, st); \
+        return i64 ? launch_tokens_t<N_, float, true>(q, grid, rpw, warps, pdl, st)             \
+                   : launch_tokens_t<N_, float, false>(q, grid, rpw, warps, pdl, st);           \
+    }
+    SSU_TOK_N(64)
+    SSU_TOK_N(128)
+    SSU_TOK_N(256)
+#undef SSU_TOK_N
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                                           const void *state_batch_indices, const uint16_t *x,
                                           const uint16_t *dt, const float *dt_bias,
@@ -54,21 +91,30 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
         return ssu_update(handle, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
                           out, shape, strides, stream);
     const ssu_shape_t &s = *shape;
-    // 8 rows per warp (4 at dstate 256), one warp per CTA (fewer rows for a small headdim), or
-    // the handle's VEC override for sweeps (16 rows per warp for dstate up to 128).
-    int rpw = s.dstate == 256 ? 4 : 8;
-    while (rpw > 1 && rpw > s.headdim) rpw >>= 1;
+    // 32 fp32 state values per lane: 8 vector rows at 4 columns per lane (fp32 at dstate 64
+    // and 128), 4 at 8 columns (dstate 256, a bf16 state); one warp per CTA.  Fewer rows for a
+    // small headdim.  The handle's VEC override (for sweeps) sets rows per warp and warps per
+    // CTA instead.
+    const int rpi = ssu_host::rows_per_instruction(s.dstate, s.state_dtype);
+    const long long row_bytes = s.dstate * (s.state_dtype == SSU_STATE_BF16 ? 2 : 4);
+    const int vpr = row_bytes >= 512 ? static_cast<int>(row_bytes / 512) : 1;  // vectors per lane
+    const int nc = (s.state_dtype == SSU_STATE_BF16 ? 8 : 4) * vpr;            // columns per lane
+    int slots = 32 / nc;
+    while (slots > 1 && slots * rpi > s.headdim) slots >>= 1;
+    int rpw = slots * rpi;
     int wpc = 1;
     if (handle->has_override && handle->override_launch.mode == SSU_MODE_VEC) {
         rpw = handle->override_launch.rows_per_warp;
         wpc = handle->override_launch.warps_per_cta;
-        if (rpw > 16 || (rpw == 16 && (s.dstate > 128 || wpc > 4)))
+        if (!ssu_host::rows_per_warp_ok(rpw, s.dstate, s.state_dtype))
+            return fail(SSU_ERR_UNSUPPORTED, "%d rows per warp do not fit dstate %lld", rpw,
+                        (long long)s.dstate);
+        if ((rpw / rpi) * nc > 64 || ((rpw / rpi) * nc > 32 && wpc > 4))
             return fail(SSU_ERR_UNSUPPORTED,
-                        "the multi-token kernel takes 1..8 rows per warp (16 with at most 4 "
-                        "warps, up to dstate 128)");
+                        "the multi-token kernel holds at most 64 state values per lane (32 in "
+                        "CTAs of more than 4 warps)");
     }
-    const int rows_per_tile = rpw * wpc;
-    const long long slabs = (s.headdim + rows_per_tile - 1) / rows_per_tile;
+    const long long slabs = (s.headdim + rpw * wpc - 1) / (rpw * wpc);
     const long long tiles = s.batch * s.nheads * slabs;
     if (tiles > INT_MAX) return fail(SSU_ERR_UNSUPPORTED, "%lld tiles exceed 2^31", tiles);
 
@@ -108,7 +154,7 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     p.heads_per_group = static_cast<int>(s.nheads / s.ngroups);
     p.group_magic = group_magic(static_cast<unsigned>(p.heads_per_group));
     p.slabs = static_cast<int>(slabs);
-    p.rows_per_cta = rows_per_tile;
+    p.rows_per_cta = rpw * wpc;
     p.err = handle->err;
     q.inter = intermediate;
     q.x_t = ts->x;
@@ -122,14 +168,14 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     q.in_p = ts->intermediate[3];
     q.tokens = static_cast<int>(tokens);
     // Whole column groups of B and C are aligned vectors when the lane's first column (a
-    // multiple of 4 columns, 2 at dstate 64) is 8-byte (4-byte) aligned at every request,
-    // token and group.
+    // multiple of the 16-byte vector's elements: 4 for an fp32 state, 8 for bf16) is 8-byte
+    // (16-byte) aligned at every request, token and group.
     {
-        const int pair = s.dstate == 64 ? 2 : 4;
-        const bool b_ok = aligned(B, 2 * pair) && strides->B[0] % pair == 0 &&
-                          strides->B[1] % pair == 0 && ts->B % pair == 0;
-        const bool c_ok = aligned(C, 2 * pair) && strides->C[0] % pair == 0 &&
-                          strides->C[1] % pair == 0 && ts->C % pair == 0;
+        const int epv = s.state_dtype == SSU_STATE_BF16 ? 8 : 4;
+        const bool b_ok = aligned(B, 2 * epv) && strides->B[0] % epv == 0 &&
+                          strides->B[1] % epv == 0 && ts->B % epv == 0;
+        const bool c_ok = aligned(C, 2 * epv) && strides->C[0] % epv == 0 &&
+                          strides->C[1] % epv == 0 && ts->C % epv == 0;
         q.bc_vec = b_ok && c_ok;
     }
 
@@ -137,12 +183,11 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     if (guard.err != cudaSuccess)
         return fail(SSU_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(guard.err));
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf16 = s.state_dtype == SSU_STATE_BF16, i64 = s.index_dtype == SSU_INDEX_I64;
     const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
                     static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
-    const int nc = static_cast<int>(s.dstate / 32);
-    const bool bf16 = s.state_dtype == SSU_STATE_BF16, i64 = s.index_dtype == SSU_INDEX_I64;
-    const cudaError_t e = launch_tokens_depth<kTokenPrefetch>(q, nc, bf16, i64, rpw, wpc, grid,
-                                                              handle->pdl, cs);
+    const cudaError_t e = launch_tokens(q, grid, static_cast<int>(s.dstate), bf16, i64, rpw,
+                                        wpc, handle->pdl, cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }

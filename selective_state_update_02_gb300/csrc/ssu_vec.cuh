@@ -1,105 +1,86 @@
 // VEC kernel of the decode step: one CTA per (slab of rows, head, request).  Each warp holds
-// RPW rows of the state in registers (all loads issued before any use), updates them, stores
-// them back in place with streaming stores and writes the readout.  Templated on the rows per
-// warp, the columns per lane (dstate = 32 * NC), the state element type (fp32 or bf16, computed
-// in fp32 either way) and the index type.
+// RPW rows of the state in registers as whole 16-byte vectors (all loads issued before any
+// use), updates them, stores them back in place with streaming stores and writes the readout.
+// Templated on the rows per warp, dstate, the state element type (fp32 or bf16, computed in
+// fp32 either way) and the index type; the lane geometry of a row is RowGeo (ssu_device.cuh).
 #pragma once
 
 #include "ssu_device.cuh"
 
 namespace {
 
-// The lane's NC columns of B (or C) widened to fp32, read as whole 4- or 8-byte column groups.
-// Only for a warp whose first column address is aligned to that width (every lane then is).
-template <int NC>
-__device__ __forceinline__ void load_bc_vec(const __nv_bfloat16 *p, float (&o)[NC]) {
-    unsigned w[NC / 2];
-    if constexpr (NC == 2) {
-        w[0] = *reinterpret_cast<const unsigned *>(p);
-    } else {
-#pragma unroll
-        for (int g = 0; g < NC / 4; ++g) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(p + g * 128);
-            w[2 * g] = u.x;
-            w[2 * g + 1] = u.y;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < NC / 2; ++i) {
-        o[2 * i] = __uint_as_float(w[i] << 16);
-        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-
 // Per-instantiation forms of the per-row work, each chosen from a same-box A/B at batch 128
 // (and 8 / 512 for fp32 at dstate 128), since the compiler's schedules differ:
 //  * kShuffleK: lane r < RPW loads x of row r and forms dt * x there; the other lanes get the
 //    product by a shuffle (instead of every lane loading every row's x and multiplying).  On
-//    for a bf16 state (dstate 128: 14.88 -> 13.78 us; 64: 11.91 -> 10.72) and for fp32 with 8
-//    rows per warp at dstate 128; off for fp32 at dstate 64 (13.26 -> 13.70) and with 2 rows
-//    per warp (batch 8: 3.56 -> 3.91).
-//  * kVectorBC: B and C read as 4- or 8-byte column groups when aligned.  On at dstate 256
-//    (bf16 26.51 -> 24.63; fp32 41.52 -> 41.14) and for fp32 with 8 rows per warp at dstate
-//    128 (both on: 22.99 -> 22.76 at batch 128, 81.03 -> 80.56 at 512); off at dstate 64
-//    (fp32 13.26 -> 14.61).
+//    wherever one instruction covers several rows (the lanes of one instruction need
+//    different rows' products), for a bf16 state, and for fp32 with 8 rows per warp at dstate
+//    128; off for fp32 with 2 rows per warp (batch 8: 3.56 -> 3.91 us with it) and at dstate
+//    256.
+//  * kVectorBC: B and C read as whole column groups (8 or 16 bytes per lane) when aligned.  On
+//    at dstate 256 (fp32 41.52 -> 41.14), for fp32 with 8 rows per warp at dstate 128 (22.99 ->
+//    22.76 at batch 128, 81.03 -> 80.56 at 512) and wherever one instruction covers several
+//    rows.
 //  * kGroupMagic: the head's group from group_of (a multiply and a shift) instead of an integer
-//    division.  On with 8 rows per warp where a lane's part of a row is one 16-byte vector
-//    (fp32 at dstate 128: 22.76 -> 22.65 at batch 128, 80.68 -> 80.53 at 512; bf16 at dstate
-//    256: 24.67 -> 24.55); off elsewhere (fp32 batch 8: 3.56 -> 3.95; bf16 dstate 128: 13.84
-//    -> 15.43; dstate 64 fp32 13.29 -> 13.74, bf16 10.74 -> 11.12; fp32 dstate 256 unchanged).
+//    division.  On with 8 rows per warp for fp32 at dstate 128 (22.76 -> 22.65 at batch 128,
+//    80.68 -> 80.53 at 512) and for bf16 at dstate 256 (24.67 -> 24.55); off for fp32 with 2
+//    rows per warp (batch 8: 3.56 -> 3.95).
 //  * kPacked: the state update in packed fp32x2 multiplies and fused multiply-adds (IEEE round
-//    to nearest per element, the same values).  On for a bf16 state (dstate 128 / 256 / 64:
-//    13.50 -> 13.42, 24.22 -> 24.07, 10.59 -> 10.47 us at batch 128) and for fp32 with 8 rows
-//    per warp at dstate 128 (22.34 -> 22.27 at batch 128, 80.17 -> 80.09 at 512); off for fp32
-//    at dstate 64 and 256 (13.00 -> 13.56, 40.94 -> 42.30: more registers, fewer warps).
+//    to nearest per element, the same values).  On for a bf16 state, for fp32 with 8 rows per
+//    warp at dstate 128 (22.34 -> 22.27 at batch 128) and wherever one instruction covers
+//    several rows; off for fp32 at dstate 256 (40.94 -> 42.30 with it: more registers, fewer
+//    warps).
 // Every combination gives the same values bit for bit.
-template <int RPW, int NC, typename ST>
+template <int RPW, int N, typename ST>
 struct VecForm {
-    static constexpr bool kShuffleK = sizeof(ST) == 2 || (NC == 4 && RPW >= 8);
-    static constexpr bool kVectorBC = NC == 8 || (NC == 4 && sizeof(ST) == 4 && RPW >= 8);
-    static constexpr bool kGroupMagic = RPW >= 8 && NC * sizeof(ST) == 16;
-    static constexpr bool kPacked = sizeof(ST) == 2 || (NC == 4 && RPW == 8);
+    using G = RowGeo<N, ST>;
+    static constexpr int S = RPW / G::RPI;  // vector instructions (slots) per warp
+    static constexpr bool kMulti = G::RPI > 1;
+    static constexpr bool kShuffleK = kMulti || sizeof(ST) == 2 || (N == 128 && RPW >= 8);
+    static constexpr bool kVectorBC = kMulti || N == 256 || (N == 128 && RPW >= 8);
+    static constexpr bool kGroupMagic = kMulti || (RPW >= 8 && G::NC * sizeof(ST) == 16);
+    static constexpr bool kPacked = kMulti || sizeof(ST) == 2 || (N == 128 && RPW == 8);
+    static_assert(RPW % G::RPI == 0 && S >= 1 && S <= G::L, "rows per warp for this dstate");
 };
 
-// update_lane (ssu_device.cuh) with the state update in packed fp32x2 instructions; the
-// readout chain stays scalar, over the columns in the same order.
-template <int NC>
-__device__ __forceinline__ float update_lane_packed(float (&v)[NC], float dA, float k,
-                                                    const float (&bb)[NC],
-                                                    const float (&cc)[NC]) {
-    const float2 k2 = make_float2(k, k), dA2 = make_float2(dA, dA);
-#pragma unroll
-    for (int i = 0; i < NC / 2; ++i) {
-        const float2 w = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), dA2,
-                                    __fmul2_rn(k2, make_float2(bb[2 * i], bb[2 * i + 1])));
-        v[2 * i] = w.x;
-        v[2 * i + 1] = w.y;
-    }
-    float part = v[0] * cc[0];
-#pragma unroll
-    for (int j = 1; j < NC; ++j) part = fmaf(v[j], cc[j], part);
-    return part;
+template <int RPW, int N, typename ST>
+__device__ __forceinline__ float update_row(float (&v)[RowGeo<N, ST>::NC], float dA, float k,
+                                            const float (&bb)[RowGeo<N, ST>::NC],
+                                            const float (&cc)[RowGeo<N, ST>::NC]) {
+    constexpr int NC = RowGeo<N, ST>::NC;
+    if constexpr (VecForm<RPW, N, ST>::kPacked)
+        return update_lane<NC>(v, dA, k, bb, cc);
+    else
+        return update_lane_scalar<NC>(v, dA, k, bb, cc);
 }
 
-template <int RPW, int NC, typename ST>
-__device__ __forceinline__ float update_row(float (&v)[NC], float dA, float k,
-                                            const float (&bb)[NC], const float (&cc)[NC]) {
-    if constexpr (VecForm<RPW, NC, ST>::kPacked)
-        return update_lane_packed<NC>(v, dA, k, bb, cc);
-    else
-        return update_lane<NC>(v, dA, k, bb, cc);
+// Registers per thread for an instantiation: the smallest multiple of 8 at which ptxas
+// (CUDA 13.0, sm_103a) keeps every variable in registers, from -Xptxas -v at each cap.  Left
+// to itself the compiler takes far more for some (fp32 dstate 64 with 16 rows per warp: 118;
+// bf16 with 8 vector rows: 103-108; fp32 dstate 256 with 4 rows: 115), which costs resident
+// warps.  At most 128, so a CTA of 16 warps always fits.
+template <int RPW, int N, typename ST>
+constexpr int vec_max_regs() {
+    using G = RowGeo<N, ST>;
+    constexpr int S = RPW / G::RPI, V = S * G::VPR;  // 16-byte vectors of state per lane
+    if constexpr (sizeof(ST) == 4) return V <= 8 ? (G::VPR == 2 && V == 8 ? 72 : 64) : 104;
+    return S <= 2 ? 64 : S <= 4 ? 72 : 96;
 }
 
 // Grid: x = slab of rows, y = head, z = request (requests beyond gridDim.z loop), so the
 // slot lookup at the head of the dependency chain needs no index arithmetic.
-template <int RPW, int NC, typename ST, bool kIdx64>
-__global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
+template <int RPW, int N, typename ST, bool kIdx64>
+__global__ void __maxnreg__((vec_max_regs<RPW, N, ST>()))
     ssu_vec_kernel(const __grid_constant__ SsuParams p) {
+    using G = RowGeo<N, ST>;
+    using F = VecForm<RPW, N, ST>;
+    constexpr int S = F::S, NC = G::NC, RPI = G::RPI;
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int slab = blockIdx.x;
     const int h = blockIdx.y;
+    const int sub = sub_of<G>(lane);
     for (long long b = blockIdx.z; b < p.batch; b += gridDim.z) {
         const long long s = load_slot<kIdx64>(p, b);
         if (s < 0 || s >= p.pool_size) {
@@ -107,19 +88,21 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
             continue;
         }
 
-        const int row0 = slab * p.rows_per_cta + warp * RPW;
+        const int row0 = slab * p.rows_per_cta + warp * RPW;  // the warp's first row
+        const int lrow = row0 + sub;                           // the lane's row in slot 0
         ST *srow = static_cast<ST *>(p.state) + s * p.st_pool + h * p.st_head +
-                   row0 * p.st_row + lane_offset<NC>(lane);
+                   lrow * p.st_row + col0_of<G>(lane);
+        const long long slot_stride = RPI * p.st_row;
 
         // Issue every state load of this warp before anything that depends on other loads.
-        float v[RPW][NC];
+        RawRow<G> raw[S];
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            if (row0 + r < p.headdim) {
-                load_cols<NC, ST>(srow + r * p.st_row, v[r]);
+        for (int r = 0; r < S; ++r) {
+            if (lrow + r * RPI < p.headdim) {
+                load_raw<G, ST>(srow + r * slot_stride, raw[r]);
             } else {
 #pragma unroll
-                for (int j = 0; j < NC; ++j) v[r][j] = 0.f;
+                for (int q = 0; q < G::VPR; ++q) raw[r].w[q] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
 
@@ -129,47 +112,64 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
         const float dtv = softplus_f32(z);
         const float dA = expf(dtv * p.A[h * p.A_h]);
         const float Dh = p.D[h * p.D_h];
-        const int g = VecForm<RPW, NC, ST>::kGroupMagic ? group_of(h, p.group_magic)
-                                                        : h / p.heads_per_group;
+        const int g = F::kGroupMagic ? group_of(h, p.group_magic) : h / p.heads_per_group;
         float bb[NC], cc[NC];
         const __nv_bfloat16 *Bw = p.B + b * p.B_b + g * p.B_g, *Cw = p.C + b * p.C_b + g * p.C_g;
-        if (VecForm<RPW, NC, ST>::kVectorBC &&
+        const bool bc_vec =
+            F::kVectorBC &&
             ((reinterpret_cast<unsigned long long>(Bw) | reinterpret_cast<unsigned long long>(Cw)) &
-             (NC == 2 ? 3u : 7u)) == 0) {
-            load_bc_vec<NC>(Bw + lane_offset<NC>(lane), bb);
-            load_bc_vec<NC>(Cw + lane_offset<NC>(lane), cc);
+             (2 * G::kEPV - 1)) == 0;
+        // Two call sites with a constant flag each: one path with the flag as a run-time
+        // argument measured 8 more registers (72 instead of 64 at 8 rows, fp32, dstate 128).
+        if (bc_vec) {
+            load_bc<G>(Bw + col0_of<G>(lane), true, bb);
+            load_bc<G>(Cw + col0_of<G>(lane), true, cc);
         } else {
-            load_bc<NC>(Bw + lane_offset<NC>(lane), bb);
-            load_bc<NC>(Cw + lane_offset<NC>(lane), cc);
+            load_bc<G>(Bw + col0_of<G>(lane), false, bb);
+            load_bc<G>(Cw + col0_of<G>(lane), false, cc);
         }
         const __nv_bfloat16 *xp = p.x + b * p.x_b + h * p.x_h + row0;
-        float part[RPW];
-        if constexpr (VecForm<RPW, NC, ST>::kShuffleK) {
+        float part[S];
+        if constexpr (F::kShuffleK) {
             const bool x_live = lane < RPW && row0 + lane < p.headdim;
             const float xl = x_live ? __bfloat162float(xp[lane]) : 0.f;
             const float kl = dtv * xl;  // lane r < RPW: dt * x of row r
 #pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                part[r] = update_row<RPW, NC, ST>(v[r], dA, __shfl_sync(0xffffffffu, kl, r), bb, cc);
-                if (row0 + r < p.headdim) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
+            for (int r = 0; r < S; ++r) {
+                float v[NC];
+                raw_to_f32<G, ST>(raw[r], v);
+                part[r] = update_row<RPW, N, ST>(v, dA, __shfl_sync(0xffffffffu, kl, r * RPI + sub),
+                                                 bb, cc);
+                if (lrow + r * RPI < p.headdim) {
+                    RawRow<G> o;
+                    f32_to_raw<G, ST>(v, o);
+                    store_raw<G, ST>(srow + r * slot_stride, o);
+                }
             }
-            const float total = reduce_rows<RPW>(part, lane);
-            const int rl = row_of_lane<RPW>(lane);
+            const float total = reduce_rows<S, G::L>(part, lane);
+            const int rl = slot_of_lane<S, G::L>(lane) * RPI + sub;  // row within the warp
             const float xr = __shfl_sync(0xffffffffu, xl, rl);
-            if (writes_row<RPW>(lane) && row0 + rl < p.headdim)
+            if (writes_row<S, G::L>(lane) && row0 + rl < p.headdim)
                 p.out[b * p.out_b + h * p.out_h + row0 + rl] =
                     __float2bfloat16_rn(fmaf(Dh, xr, total));
         } else {
+            static_assert(RPI == 1, "several rows per instruction need the shuffled dt * x");
 #pragma unroll
-            for (int r = 0; r < RPW; ++r) {
+            for (int r = 0; r < S; ++r) {
                 const bool live = row0 + r < p.headdim;
                 const float xr = live ? __bfloat162float(xp[r]) : 0.f;
-                part[r] = update_row<RPW, NC, ST>(v[r], dA, dtv * xr, bb, cc);
-                if (live) store_cols<NC, ST>(srow + r * p.st_row, v[r]);
+                float v[NC];
+                raw_to_f32<G, ST>(raw[r], v);
+                part[r] = update_row<RPW, N, ST>(v, dA, dtv * xr, bb, cc);
+                if (live) {
+                    RawRow<G> o;
+                    f32_to_raw<G, ST>(v, o);
+                    store_raw<G, ST>(srow + r * slot_stride, o);
+                }
             }
-            const float total = reduce_rows<RPW>(part, lane);
-            const int rl = row_of_lane<RPW>(lane);
-            if (writes_row<RPW>(lane) && row0 + rl < p.headdim) {
+            const float total = reduce_rows<S, G::L>(part, lane);
+            const int rl = slot_of_lane<S, G::L>(lane);
+            if (writes_row<S, G::L>(lane) && row0 + rl < p.headdim) {
                 const float xr = __bfloat162float(xp[rl]);
                 p.out[b * p.out_b + h * p.out_h + row0 + rl] =
                     __float2bfloat16_rn(fmaf(Dh, xr, total));
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
 
 // Launches one instantiation; with `pdl` the launch may begin before the previous kernel in
 // the stream has finished (the kernel waits for it before touching memory).
-template <int RPW, int NC, typename ST, bool kIdx64>
+template <int RPW, int N, typename ST, bool kIdx64>
 cudaError_t launch_vec_one(const SsuParams &p, dim3 grid, dim3 block, bool pdl, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -192,42 +192,41 @@ cudaError_t launch_vec_one(const SsuParams &p, dim3 grid, dim3 block, bool pdl, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, ssu_vec_kernel<RPW, NC, ST, kIdx64>, p);
+    return cudaLaunchKernelEx(&cfg, ssu_vec_kernel<RPW, N, ST, kIdx64>, p);
 }
 
-template <int NC, typename ST, bool kIdx64>
+// Rows per warp this build instantiates for a (dstate, state type): RPI x {1, 2, 4, 8}, and 16
+// for an fp32 state of dstate 128.
+template <int N, typename ST, bool kIdx64>
 cudaError_t launch_vec_t(const SsuParams &p, int rpw, int wpc, dim3 grid, bool pdl,
                          cudaStream_t st) {
+    constexpr int RPI = RowGeo<N, ST>::RPI;
     const dim3 block(32 * wpc);
-    switch (rpw) {
-        case 1: return launch_vec_one<1, NC, ST, kIdx64>(p, grid, block, pdl, st);
-        case 2: return launch_vec_one<2, NC, ST, kIdx64>(p, grid, block, pdl, st);
-        case 4: return launch_vec_one<4, NC, ST, kIdx64>(p, grid, block, pdl, st);
-        case 8: return launch_vec_one<8, NC, ST, kIdx64>(p, grid, block, pdl, st);
-        case 16:
-            if constexpr (NC == 4 && sizeof(ST) == 4)
-                return launch_vec_one<16, NC, ST, kIdx64>(p, grid, block, pdl, st);
-            else
-                return cudaErrorInvalidValue;
-        default: return cudaErrorInvalidValue;
-    }
+    if (rpw == RPI) return launch_vec_one<RPI, N, ST, kIdx64>(p, grid, block, pdl, st);
+    if (rpw == 2 * RPI) return launch_vec_one<2 * RPI, N, ST, kIdx64>(p, grid, block, pdl, st);
+    if (rpw == 4 * RPI) return launch_vec_one<4 * RPI, N, ST, kIdx64>(p, grid, block, pdl, st);
+    if (rpw == 8 * RPI) return launch_vec_one<8 * RPI, N, ST, kIdx64>(p, grid, block, pdl, st);
+    if constexpr (N == 128 && sizeof(ST) == 4)
+        if (rpw == 16) return launch_vec_one<16, N, ST, kIdx64>(p, grid, block, pdl, st);
+    return cudaErrorInvalidValue;
 }
 
-// Launches the VEC kernel for dstate = 32 * nc, a bf16 or fp32 state, int64 or int32 indices.
-inline cudaError_t launch_vec(const SsuParams &p, int nc, bool bf16, bool i64, int rpw, int wpc,
-                              dim3 grid, bool pdl, cudaStream_t st) {
-#define SSU_VEC_NC(NC_)                                                                     \
-    if (nc == NC_) {                                                                        \
-        if (bf16)                                                                           \
-            return i64 ? launch_vec_t<NC_, __nv_bfloat16, true>(p, rpw, wpc, grid, pdl, st) \
-                       : launch_vec_t<NC_, __nv_bfloat16, false>(p, rpw, wpc, grid, pdl, st); \
-        return i64 ? launch_vec_t<NC_, float, true>(p, rpw, wpc, grid, pdl, st)             \
-                   : launch_vec_t<NC_, float, false>(p, rpw, wpc, grid, pdl, st);           \
+// Launches the VEC kernel for dstate 64, 128 or 256, a bf16 or fp32 state, int64 or int32
+// indices.
+inline cudaError_t launch_vec(const SsuParams &p, int dstate, bool bf16, bool i64, int rpw,
+                              int wpc, dim3 grid, bool pdl, cudaStream_t st) {
+#define SSU_VEC_N(N_)                                                                      \
+    if (dstate == N_) {                                                                    \
+        if (bf16)                                                                          \
+            return i64 ? launch_vec_t<N_, __nv_bfloat16, true>(p, rpw, wpc, grid, pdl, st) \
+                       : launch_vec_t<N_, __nv_bfloat16, false>(p, rpw, wpc, grid, pdl, st); \
+        return i64 ? launch_vec_t<N_, float, true>(p, rpw, wpc, grid, pdl, st)             \
+                   : launch_vec_t<N_, float, false>(p, rpw, wpc, grid, pdl, st);           \
     }
-    SSU_VEC_NC(2)
-    SSU_VEC_NC(4)
-    SSU_VEC_NC(8)
-#undef SSU_VEC_NC
+    SSU_VEC_N(64)
+    SSU_VEC_N(128)
+    SSU_VEC_N(256)
+#undef SSU_VEC_N
     return cudaErrorInvalidValue;
 }
 

@@ -34,7 +34,7 @@ def declared_functions() -> list[str]:
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("ssu_create", "ssu_update", "ssu_destroy", "ssu_get_error", "ssu_validate",
-                 "ssu_set_launch", "ssu_get_launch"):
+                 "ssu_set_launch", "ssu_set_launch_override", "ssu_get_launch"):
         assert must in names
 
 
@@ -54,7 +54,7 @@ def test_binding_covers_every_declared_function(ssu):
 
 
 def test_version_and_status_strings(ssu):
-    assert ssu.ssu_abi_version() == 1
+    assert ssu.ssu_abi_version() == 2 == ssu.SSU_ABI_VERSION
     assert ssu.status_string(ssu.SSU_ERR_MISALIGNED) == "SSU_ERR_MISALIGNED"
     assert ssu.status_string(99) == "SSU_ERR_UNKNOWN"
 
@@ -150,7 +150,23 @@ def test_null_handle_is_rejected_before_any_cuda_call(ssu):
     ptrs, shape, st = canonical()
     assert ssu.ssu_update_raw(None, ptrs, shape, st, None) == ssu.SSU_ERR_INVALID_ARG
     assert ssu.lib().ssu_set_launch(None, None) == ssu.SSU_ERR_INVALID_ARG
+    assert ssu.lib().ssu_set_launch_override(None, b"8,4") == ssu.SSU_ERR_INVALID_ARG
     assert ssu.lib().ssu_destroy(None) == ssu.SSU_OK
+
+
+def test_static_counters_out_is_checked_before_the_call(ssu):
+    # counters_out receives a 12-byte device copy: a CPU tensor, a 2-byte dtype, a float
+    # dtype or fewer than 3 elements are refused in Python, before the library is called.
+    bs, H, P, N = 2, 2, 8, 128
+    pool = torch.zeros(4, H, P, N)
+    x = torch.zeros(bs, H, P, dtype=torch.bfloat16)
+    bc = torch.zeros(bs, 1, N, dtype=torch.bfloat16)
+    args = (pool, torch.arange(bs, dtype=torch.int32), x, torch.zeros(bs, H, dtype=torch.bfloat16),
+            torch.zeros(H), torch.zeros(H), bc, bc, torch.zeros(H), torch.zeros_like(x))
+    for bad in (torch.zeros(3, dtype=torch.int32), torch.zeros(3, dtype=torch.int16),
+                torch.zeros(3, dtype=torch.float32), torch.zeros(2, dtype=torch.int32)):
+        with pytest.raises(ValueError):
+            ssu.ssu_update_static(*args, counters_out=bad)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

@@ -131,3 +131,18 @@ def test_token_bytes_reduce_to_single_step():
     assert extra == 128 * (16 * 64 * 2 * 2 + 2 * 128 * 2 + 16 * 2)
     assert (bench.bytes_per_call_tokens(128, 3, True) - bench.bytes_per_call_tokens(128, 3, False)
             == 3 * 128 * 16 * 64 * 128 * 4)
+
+
+def test_reference_arm_and_cpu_baseline_time_the_oracle_alike(capsys):
+    # Both legs time the oracle with one routine (oracle_call_us: the oracle call alone, one
+    # persistent thread pool, median over calls), so on the same host they agree; they
+    # differed 3.4x when the reference arm's timed loop also held a copy of the pool per step.
+    import argparse
+    bs = 32
+    base = bench.cpu_baseline(bs, 16, budget_s=1.0)
+    args = argparse.Namespace(gpus=1, steps=6, warmup=1, batch=bs)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    ratio = line["value"] / base["value"]
+    assert 0.6 < ratio < 1.6, (line["value"], base["value"])
+    assert line["cpu_baseline"]["cores"] == base["cores"]

@@ -4,6 +4,8 @@ step, skipped requests, and a sampled serving-size batch."""
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -57,14 +59,20 @@ def test_single_step(op, N, dtype, P):
     _compare_all(pr, t)
 
 
+def rows_per_instruction(N: int, dtype: str) -> int:
+    """Rows one warp-wide 16-byte vector instruction covers: 512 bytes of state."""
+    return max(1, 512 // (N * (2 if dtype == "bf16" else 4)))
+
+
 @pytest.mark.parametrize("N,dtype", COMBOS)
 def test_every_vec_shape_is_bitwise_identical(op, N, dtype):
     pr = wl.make_problem(6, 16, P=40, N=N, pool_size=14, seed=7, state_dtype=dtype)
     ref = to_device(pr)
     _run(op, ref)
     _compare_all(pr, ref)
+    rpi = rows_per_instruction(N, dtype)
     try:
-        for rpw in (1, 2, 4, 8):
+        for rpw in (rpi, 2 * rpi, 4 * rpi, 8 * rpi):
             for wpc in (1, 2, 3, 4, 8):
                 t = to_device(pr)
                 op.set_launch(ssu.SSU_MODE_VEC, rpw, wpc)
@@ -79,17 +87,59 @@ def test_every_vec_shape_is_bitwise_identical(op, N, dtype):
 
 
 @pytest.mark.parametrize("N,dtype", COMBOS)
-def test_bulk_and_16_rows_are_refused_outside_fp32_128(op, N, dtype):
+def test_rows_per_warp_outside_the_bucket_are_refused(op, N, dtype):
+    # A warp's rows come in whole vector instructions (rows_per_instruction of them) and at
+    # most 8 instructions per warp (16 rows only for an fp32 state of dstate 128).
     pr = wl.make_problem(4, 8, N=N, pool_size=8, seed=2, state_dtype=dtype)
     t = to_device(pr)
-    for shape in ((ssu.SSU_MODE_BULK, 8, 4, 2), (ssu.SSU_MODE_VEC, 16, 2, 0)):
-        op.set_launch(*shape)
+    rpi = rows_per_instruction(N, dtype)
+    bad = [16 * rpi] + ([rpi // 2] if rpi > 1 else [])
+    for rpw in bad:
         try:
+            # refused when set (more than 32 rows per warp) or at the call (not a shape of
+            # this bucket)
             with pytest.raises(ssu.SsuError) as e:
+                op.set_launch(ssu.SSU_MODE_VEC, rpw, 2)
                 _run(op, t)
             assert e.value.status == ssu.SSU_ERR_UNSUPPORTED
         finally:
             op.set_launch(ssu.SSU_MODE_AUTO)
+
+
+@pytest.mark.parametrize("N,dtype", COMBOS + [(128, "f32")])
+def test_every_token_shape_is_bitwise_identical(op, N, dtype):
+    # The multi-token kernel's tiles (rows per warp, warps per CTA) change which warp updates
+    # which rows, never the arithmetic: every shape gives the bits of the table's shape.
+    bs, T, H, P = 9, 3, 8, 40
+    pr = wl.make_problem(bs, H, P=P, N=N, pool_size=12, seed=19, state_dtype=dtype)
+    rng = np.random.default_rng(20)
+    steps = [wl.request_inputs(rng, bs, H, P, N) for _ in range(T)]
+    x, dt, B, C = (bf16_tensor(np.stack([s[k] for s in steps], 1), "cuda") for k in range(4))
+
+    def run():
+        dev = to_device(pr)
+        out = torch.zeros(bs, T, H, P, dtype=torch.bfloat16, device="cuda")
+        op.tokens(dev["state_pool"], dev["state_batch_indices"], x, dt, dev["dt_bias"],
+                  dev["A"], B, C, dev["D"], out)
+        torch.cuda.synchronize()
+        return dev["state_pool"].view(torch.int16).clone() if dtype == "bf16" else \
+            dev["state_pool"].clone(), out.view(torch.int16).clone()
+
+    ref_pool, ref_out = run()
+    rpi = rows_per_instruction(N, dtype)
+    nc = 8 if (dtype == "bf16" or N == 256) else 4
+    try:
+        for slots in (1, 2, 4, 8):
+            if slots * nc > 32:
+                continue
+            for wpc in (1, 2, 4):
+                op.set_launch(ssu.SSU_MODE_VEC, slots * rpi, wpc)
+                got_pool, got_out = run()
+                assert torch.equal(got_pool, ref_pool), (slots * rpi, wpc)
+                assert torch.equal(got_out, ref_out), (slots * rpi, wpc)
+    finally:
+        op.set_launch(ssu.SSU_MODE_AUTO)
+    assert op.get_error() == (0, -1)
 
 
 @pytest.mark.parametrize("N,dtype", COMBOS)
@@ -134,7 +184,7 @@ def test_tokens(op, N, dtype):
                                      (64, "bf16")])
 def test_serving_batch_128_sampled(op, N, dtype):
     """Each bucket at the batch the bench times it (128 requests, 16 heads, the built-in
-    launch table), slots scattered over a 384-slot pool; sampled requests against the oracle,
+    launch table), slots scattered over a 384-slot pool; every request against the oracle,
     every other slot unchanged."""
     bs, H, slots = 128, 16, 384
     rng = np.random.default_rng(5 + N)
@@ -148,8 +198,9 @@ def test_serving_batch_128_sampled(op, N, dtype):
        torch.from_numpy(dt_bias).cuda(), torch.from_numpy(A).cuda(), bf16_tensor(B, "cuda"),
        bf16_tensor(C, "cuda"), torch.from_numpy(D).cuda(), out)
     torch.cuda.synchronize()
-    rows = np.array([0, 3, 77, 127])
-    ref_states, ref_y = oracle_on_requests(pool, idx, rows, x, dt, dt_bias, A, B, C, D)
+    rows = np.arange(bs)  # every request against the oracle
+    ref_states, ref_y = oracle_on_requests(pool, idx, rows, x, dt, dt_bias, A, B, C, D,
+                                           threads=os.cpu_count() or 1)
     got = pool_host(pool_d)
     check_state(got[idx[rows]], ref_states)
     Ch, Dx = expected_terms(x[rows], D, C[rows], 1, H)
@@ -157,3 +208,24 @@ def test_serving_batch_128_sampled(op, N, dtype):
     mask = np.ones(slots, bool)
     mask[idx] = False
     assert np.array_equal(got[mask], pool[mask])
+
+
+@pytest.mark.parametrize("N,dtype", COMBOS)
+def test_one_token_kernel_equals_ssu_update_bitwise(op, N, dtype):
+    """T = 1 with an intermediate buffer runs the multi-token kernel; it gives the bits of
+    ssu_update in every bucket (one element mapping, one summation order)."""
+    bs, H, P = 11, 8, 40
+    pr = wl.make_problem(bs, H, P=P, N=N, pool_size=15, seed=23, state_dtype=dtype)
+    a, b = to_device(pr), to_device(pr)
+    _run(op, a)
+    out = torch.zeros(bs, 1, H, P, dtype=torch.bfloat16, device="cuda")
+    inter = torch.zeros(bs, 1, H, P, N, dtype=b["state_pool"].dtype, device="cuda")
+    op.tokens(b["state_pool"], b["state_batch_indices"], b["x"].unsqueeze(1),
+              b["dt"].unsqueeze(1), b["dt_bias"], b["A"], b["B"].unsqueeze(1),
+              b["C"].unsqueeze(1), b["D"], out, inter)
+    torch.cuda.synchronize()
+    as_bits = (lambda t: t.view(torch.int16)) if dtype == "bf16" else (lambda t: t)
+    assert torch.equal(as_bits(a["state_pool"]), as_bits(b["state_pool"]))
+    assert torch.equal(a["out"].view(torch.int16), out[:, 0].view(torch.int16))
+    idx = torch.from_numpy(pr.idx).cuda()
+    assert torch.equal(as_bits(inter[:, 0]), as_bits(b["state_pool"][idx]))

@@ -70,15 +70,13 @@ def test_copy_matches_oracle(op, idx_dtype):
     assert skipped == 0 and op.get_error() == (0, -1)
 
 
-COPY_SHAPES = ([(ssu.SSU_COPY_VEC, c, v, t) for c in (4, 8, 16, 32, 64) for v in (1, 2, 4, 8, 16)
-                for t in (64, 256)] +
-               [(ssu.SSU_COPY_BULK, c, st, 0) for c in (4, 8, 16, 32, 64) for st in (3, 4, 6)
-                if 128 + st * c * 1024 <= 220 * 1024])
+COPY_SHAPES = [(ssu.SSU_COPY_VEC, c, v, t) for c in (4, 8, 16, 32, 64) for v in (1, 2, 4, 8, 16)
+               for t in (64, 256)]
 
 
-def test_oversized_bulk_ring_is_refused(op):
+def test_unknown_copy_mode_is_refused(op):
     with pytest.raises(ssu.SsuError) as e:
-        ssu.ssu_copy_set_launch(op.handle, ssu.SSU_COPY_BULK, 64, 6, 0)
+        ssu.ssu_copy_set_launch(op.handle, 2, 64, 6, 0)
     assert e.value.status == ssu.SSU_ERR_UNSUPPORTED
 
 
@@ -93,9 +91,9 @@ def test_every_copy_shape(op):
         ssu.ssu_copy_set_launch(op.handle, ssu.SSU_COPY_AUTO)
 
 
-@pytest.mark.parametrize("mode", [ssu.SSU_COPY_VEC, ssu.SSU_COPY_BULK])
-def test_copy_skips_out_of_range_requests(op, mode):
-    ssu.ssu_copy_set_launch(op.handle, mode, 8, 4 if mode == ssu.SSU_COPY_BULK else 8, 256)
+@pytest.mark.parametrize("vectors", [1, 8])
+def test_copy_skips_out_of_range_requests(op, vectors):
+    ssu.ssu_copy_set_launch(op.handle, ssu.SSU_COPY_VEC, 8, vectors, 256)
     try:
         # request 1: dst out of range; request 3: negative src
         skipped = _run_and_compare(op, SPECS, [0, 1, 2, -1, 4], [5, 12, 6, 7, 8])

@@ -14,8 +14,8 @@ import torch
 
 import selective_state_update_02_gb300 as ssu
 import workloads as wl
-from parity_util import (bf16_tensor, bits_of, check_state, check_y, expected_terms,
-                         oracle_on_requests, to_device)
+from parity_util import (bf16_tensor, bits_of, check_state, check_y, compare_every_request,
+                         expected_terms, oracle_on_requests, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -77,9 +77,7 @@ def test_groups(op, H, G):
 
 
 VEC_SHAPES = [(ssu.SSU_MODE_VEC, r, w, 0) for r in (1, 2, 4, 8, 16) for w in (1, 2, 3, 4, 8, 16)]
-BULK_SHAPES = [(ssu.SSU_MODE_BULK, r, w, st) for r in (2, 4, 8, 16) for w in (1, 2, 3, 4, 8)
-               for st in (2, 3, 5) if st * r * w * 512 <= 200 * 1024]
-SHAPES = VEC_SHAPES + BULK_SHAPES
+SHAPES = VEC_SHAPES
 
 
 @pytest.mark.parametrize("P", [64, 40])
@@ -119,12 +117,11 @@ def test_every_vec_shape_with_groups(op, H, G):
         op.set_launch(ssu.SSU_MODE_AUTO)
 
 
-@pytest.mark.parametrize("shape", [(ssu.SSU_MODE_BULK, 8, 4, 4), (ssu.SSU_MODE_BULK, 2, 1, 2),
-                                   (ssu.SSU_MODE_BULK, 16, 8, 3)])
+@pytest.mark.parametrize("shape", [(ssu.SSU_MODE_VEC, 8, 4, 0), (ssu.SSU_MODE_VEC, 2, 1, 0),
+                                   (ssu.SSU_MODE_VEC, 16, 4, 0)])
 @pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
-def test_bulk_pipeline_many_tiles_per_cta(op, shape, idx_dtype):
-    # A batch large enough that every persistent CTA streams many tiles through its ring
-    # (several wraps of every stage), compared with the oracle on sampled requests.
+def test_many_requests_every_request_checked(op, shape, idx_dtype):
+    # 96 requests (several waves of CTAs at every shape), every request against the oracle.
     bs, H = 96, 16
     pr = wl.make_problem(bs, H, pool_size=bs + 16, seed=17)
     t = to_device(pr, DEV, idx_dtype)
@@ -137,7 +134,7 @@ def test_bulk_pipeline_many_tiles_per_cta(op, shape, idx_dtype):
     _compare_all(pr, t, pr.pool)
 
 
-def test_bulk_skips_out_of_range_slots(op):
+def test_skipped_slots_among_many_requests(op):
     pr = wl.make_problem(40, 16, pool_size=48, seed=23)
     idx = pr.idx.copy()
     bad = [0, 5, 39]
@@ -145,12 +142,8 @@ def test_bulk_skips_out_of_range_slots(op):
     t = to_device(pr, DEV)
     t["state_batch_indices"] = torch.from_numpy(idx).to(DEV).to(torch.int32)
     t["out"].fill_(3.0)
-    op.set_launch(ssu.SSU_MODE_BULK, 8, 4, 3)
-    try:
-        _run(op, t)
-        assert op.get_error() == (3, 0)
-    finally:
-        op.set_launch(ssu.SSU_MODE_AUTO)
+    _run(op, t)
+    assert op.get_error() == (3, 0)
     good = np.setdiff1d(np.arange(40), bad)
     assert (t["out"][bad].float() == 3.0).all()
     ref_states, ref_y = oracle_on_requests(pr.pool, idx, good, pr.x, pr.dt, pr.dt_bias, pr.A,
@@ -163,21 +156,14 @@ def test_bulk_skips_out_of_range_slots(op):
     check_y(bits_of(t["out"])[good], ref_y, ref_states, Ch, Dx, 128)
 
 
-def test_bulk_needs_contiguous_rows(op):
-    # rows padded to 132 floats: the bulk copy of a tile would cover the padding, so a forced
-    # BULK shape is refused and the table path (VEC) still gives the right answer.
+def test_padded_rows_leave_the_padding_alone(op):
+    # rows padded to 132 floats (row stride 132): the update reads and writes the 128 columns
+    # of each row only; the padding stays zero.
     pr = wl.make_problem(4, 16, pool_size=8, seed=29)
     padded = torch.zeros(8, 16, 64, 132, device=DEV)
     padded[..., :128] = torch.from_numpy(pr.pool).to(DEV)
     t = to_device(pr, DEV)
     t["state_pool"] = padded[..., :128]
-    op.set_launch(ssu.SSU_MODE_BULK, 8, 4, 3)
-    try:
-        with pytest.raises(ssu.SsuError) as e:
-            _run(op, t)
-        assert e.value.status == ssu.SSU_ERR_UNSUPPORTED
-    finally:
-        op.set_launch(ssu.SSU_MODE_AUTO)
     _run(op, t)
     _compare_all(pr, dict(t, state_pool=t["state_pool"]), pr.pool)
     assert (padded[..., 128:] == 0).all()
@@ -271,21 +257,7 @@ def test_invalid_arguments_are_rejected_before_launch(op):
     assert e.value.status == ssu.SSU_ERR_MISALIGNED
 
 
-# ---- full-size workloads (sampled) ------------------------------------------------------
-
-def _sampled_check(pr_pool, idx, rows, x, dt, dt_bias, A, B, C, D, got_pool_rows, got_out_rows,
-                   H, G=1):
-    ref_states, ref_y = oracle_on_requests(pr_pool, idx, rows, x, dt, dt_bias, A, B, C, D, G)
-    check_state(got_pool_rows, ref_states)
-    Ch, Dx = expected_terms(x[rows], D, C[rows], G, H)
-    return check_y(got_out_rows, ref_y, ref_states, Ch, Dx, 128)
-
-
-def _sample_rows(bs, k, seed):
-    rng = np.random.default_rng(seed)
-    pick = set([0, bs - 1]) | set(rng.choice(bs, size=min(k, bs), replace=False).tolist())
-    return np.array(sorted(pick))
-
+# ---- full-size workloads (every request against the oracle) ---------------------------
 
 def test_serving_batch_128_rotation_pool(op):
     # batch 128, 16 heads: 2432-slot pool in 19 disjoint 128-slot sets (>= 3x L2); two
@@ -303,9 +275,8 @@ def test_serving_batch_128_rotation_pool(op):
         op(pool_d, torch.from_numpy(idx.astype(np.int32)).to(DEV), bf16_tensor(x, DEV),
            bf16_tensor(dt, DEV), torch.from_numpy(dt_bias).to(DEV), torch.from_numpy(A).to(DEV),
            bf16_tensor(B, DEV), bf16_tensor(C, DEV), torch.from_numpy(D).to(DEV), out)
-        rows = _sample_rows(bs, 24, k)
-        got = pool_d[torch.from_numpy(idx[rows]).to(DEV)].cpu().numpy()
-        _sampled_check(pool, idx, rows, x, dt, dt_bias, A, B, C, D, got, bits_of(out)[rows], H)
+        # every request against the oracle
+        compare_every_request(pool, idx, x, dt, dt_bias, A, B, C, D, pool_d, bits_of(out))
         assert torch.isfinite(out.float()).all()
         # untouched slots stay bit-identical; the host copy tracks the expected pool
         mask = np.ones(pool.shape[0], bool)
@@ -338,12 +309,11 @@ def test_large_batch_512_packed_views(op):
     idx = sets[2]
     out = torch.zeros(bs, H, P, dtype=torch.bfloat16, device=DEV)
     op(pool_d, torch.from_numpy(idx).to(DEV), x_v, dt_v, bias_v, A_v, B_v, C_v, D_v, out)
-    rows = _sample_rows(bs, 24, 7)
-    xs = packed[:, :H * P].reshape(bs, H, P)
-    Bs = packed[:, H * P:H * P + N].reshape(bs, 1, N)
-    Cs = packed[:, H * P + N:].reshape(bs, 1, N)
-    got = pool_d[torch.from_numpy(idx[rows]).to(DEV)].cpu().numpy()
-    _sampled_check(pool, idx, rows, xs, dt, dt_bias, A, Bs, Cs, D, got, bits_of(out)[rows], H)
+    xs = np.ascontiguousarray(packed[:, :H * P].reshape(bs, H, P))
+    Bs = np.ascontiguousarray(packed[:, H * P:H * P + N].reshape(bs, 1, N))
+    Cs = np.ascontiguousarray(packed[:, H * P + N:].reshape(bs, 1, N))
+    # every request against the oracle
+    compare_every_request(pool, idx, xs, dt, dt_bias, A, Bs, Cs, D, pool_d, bits_of(out))
     mask = np.ones(pool.shape[0], bool)
     mask[idx] = False
     keep = torch.from_numpy(np.nonzero(mask)[0]).to(DEV)
@@ -365,9 +335,9 @@ def test_head_sweep_batch_256(op, H):
     op(pool_d, torch.from_numpy(idx).to(DEV), bf16_tensor(x, DEV), bf16_tensor(dt, DEV),
        torch.from_numpy(dt_bias).to(DEV), torch.from_numpy(A).to(DEV), bf16_tensor(B, DEV),
        bf16_tensor(C, DEV), torch.from_numpy(D).to(DEV), out)
-    rows = _sample_rows(bs, 12, H)
-    got = pool_d[torch.from_numpy(idx[rows]).to(DEV)].cpu().numpy()
-    _sampled_check(pool, idx, rows, x, dt, dt_bias, A, B, C, D, got, bits_of(out)[rows], H)
+    # every request against the oracle, 16 at a time (128 heads: 1 GiB of fp64 per chunk)
+    compare_every_request(pool, idx, x, dt, dt_bias, A, B, C, D, pool_d, bits_of(out),
+                          chunk=max(1, 2048 // H))
     mask = np.ones(pool.shape[0], bool)
     mask[idx] = False
     keep = torch.from_numpy(np.nonzero(mask)[0]).to(DEV)
@@ -462,3 +432,45 @@ def test_degenerate_value_regimes(op):
     _run(op, t)
     assert op.get_error() == (0, -1)
     _compare_all(pr, t, pr.pool)
+
+
+def test_launch_override_from_text_and_environment(monkeypatch):
+    # "rows,warps" (optionally "vec,rows,warps") forces a shape, "auto"/""/None restores the
+    # table; malformed text and shapes the kernels lack are refused and change nothing.  The
+    # same text in SSU_LAUNCH is a new handle's initial override; unparsable text there makes
+    # ssu_create fail.
+    pr = wl.make_problem(5, 16, pool_size=9, seed=13)
+    base = ssu.SelectiveStateUpdate(0)
+    try:
+        t = to_device(pr, DEV)
+        shp, _ = ssu.describe(t["state_pool"], t["state_batch_indices"], t["x"], t["dt"],
+                              t["dt_bias"], t["A"], t["B"], t["C"], t["D"], t["out"])
+        table = ssu.ssu_get_launch(base.handle, shp)
+        for text, want in (("8,4", (1, 8, 4, 0)), (" vec, 2 ,16", (1, 2, 16, 0)),
+                           ("VEC,1,1", (1, 1, 1, 0)), ("auto", table), ("", table),
+                           (None, table)):
+            ssu.ssu_set_launch_override(base.handle, text)
+            assert ssu.ssu_get_launch(base.handle, shp) == want, text
+        ssu.ssu_set_launch_override(base.handle, "4,2")
+        for bad, status in (("8", ssu.SSU_ERR_INVALID_ARG), ("8,", ssu.SSU_ERR_INVALID_ARG),
+                            ("x,8,4", ssu.SSU_ERR_INVALID_ARG), ("8,4,2", ssu.SSU_ERR_INVALID_ARG),
+                            ("3,4", ssu.SSU_ERR_UNSUPPORTED), ("8,17", ssu.SSU_ERR_UNSUPPORTED),
+                            ("-8,4", ssu.SSU_ERR_INVALID_ARG)):
+            with pytest.raises(ssu.SsuError) as e:
+                ssu.ssu_set_launch_override(base.handle, bad)
+            assert e.value.status == status, bad
+            assert ssu.ssu_get_launch(base.handle, shp) == (1, 4, 2, 0), bad
+        _run(base, t)
+        _compare_all(pr, t, pr.pool)
+    finally:
+        base.close()
+    monkeypatch.setenv("SSU_LAUNCH", "2,8")
+    h = ssu.ssu_create(0)
+    try:
+        assert ssu.ssu_get_launch(h, shp) == (1, 2, 8, 0)
+    finally:
+        ssu.ssu_destroy(h)
+    monkeypatch.setenv("SSU_LAUNCH", "eight,four")
+    with pytest.raises(ssu.SsuError) as e:
+        ssu.ssu_create(0)
+    assert e.value.status == ssu.SSU_ERR_INVALID_ARG

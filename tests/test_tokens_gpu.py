@@ -139,9 +139,10 @@ def test_tokens_strided_views(op):
     _check_all(pr, x, dt, B, C, dev["state_pool"].cpu().numpy(), bits_of(out), None)
 
 
-def test_tokens_serving_batch_128_sampled(op):
+def test_tokens_serving_batch_128_every_request(op):
     # batch 128, 16 heads, 3 tokens per request (one verified token plus two drafts), a
-    # 2432-slot pool; sampled requests against the oracle, untouched slots bit-identical.
+    # 2432-slot pool: every request's state, readouts and intermediate states against the
+    # oracle (in chunks of 32 requests), untouched slots bit-identical.
     bs, T, H = 128, 3, 16
     rng = np.random.default_rng(3)
     pool = wl.state_pool(rng, 2432, H)
@@ -156,30 +157,48 @@ def test_tokens_serving_batch_128_sampled(op):
               torch.from_numpy(dt_bias).cuda(), torch.from_numpy(A).cuda(), bf16_tensor(B, "cuda"),
               bf16_tensor(C, "cuda"), torch.from_numpy(D).cuda(), out, inter)
     torch.cuda.synchronize()
-    rows = np.array([0, 17, 64, 127])
-    sub = pool[idx[rows]]
-    ref_pool, ref_y, ref_inter, _ = oracle.ssu_tokens(sub, np.arange(len(rows)), x[rows],
-                                                     dt[rows], dt_bias, A, B[rows], C[rows], D)
-    got_pool = pool_d[torch.from_numpy(idx[rows]).cuda()].cpu().numpy()
-    check_state(got_pool, ref_pool)
-    got_inter = inter[torch.from_numpy(rows).cuda()].cpu().numpy()
-    got_out = bits_of(out)[rows]
-    for t in range(T):
-        check_state(got_inter[:, t], ref_inter[:, t])
-        Ch, Dx = expected_terms(x[rows, t], D, C[rows, t], 1, H)
-        check_y(got_out[:, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, 128)
+    out_bits = bits_of(out)
+    for lo in range(0, bs, 32):
+        rows = np.arange(lo, lo + 32)
+        sub = pool[idx[rows]]
+        ref_pool, ref_y, ref_inter, _ = oracle.ssu_tokens(sub, np.arange(len(rows)), x[rows],
+                                                         dt[rows], dt_bias, A, B[rows], C[rows],
+                                                         D)
+        got_pool = pool_d[torch.from_numpy(idx[rows]).cuda()].cpu().numpy()
+        check_state(got_pool, ref_pool)
+        got_inter = inter[torch.from_numpy(rows).cuda()].cpu().numpy()
+        for t in range(T):
+            check_state(got_inter[:, t], ref_inter[:, t])
+            Ch, Dx = expected_terms(x[rows, t], D, C[rows, t], 1, H)
+            check_y(out_bits[rows, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, 128)
     mask = np.ones(2432, bool)
     mask[idx] = False
     keep = torch.from_numpy(np.nonzero(mask)[0]).cuda()
     assert torch.equal(pool_d[keep], torch.from_numpy(pool[mask]).cuda())
 
 
+@pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
+def test_tokens_many_tiles_per_warp_with_skips(op, idx_dtype):
+    """Enough tiles that every persistent warp takes many (its shared-memory ring wraps over
+    and over), with skipped requests scattered among them: every request against the oracle,
+    the skipped ones counted and left alone."""
+    bs, T, H = 300, 2, 16
+    pr, x, dt, B, C = _tokens_problem(bs, T, H=H, pool_size=bs + 40, seed=41)
+    idx = pr.idx.copy()
+    bad = [0, 7, 150, 151, 299]
+    idx[bad] = [bs + 40, -1, -5, 1 << 30, bs + 41]
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, idx=idx, idx_dtype=idx_dtype)
+    skipped = _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter, idx=idx)
+    assert skipped == len(bad)
+    assert op.get_error() == (len(bad), 0)
+    assert (got_inter[bad] == 123.0).all()
+
 
 @pytest.mark.parametrize("T,N", [(2, 128), (5, 128), (3, 64), (4, 256)])
 def test_unaligned_B_C_take_the_scalar_loads_with_the_same_bits(op, T, N):
     """B and C one element past an 8-byte boundary (only 2-byte aligned) cannot be read as
     column vectors; the kernel then loads them element by element.  Both forms must give the
-    same bits, with the 2-token (T <= 2) and the 4-token (T >= 3) prefetch rings."""
+    same bits, at several token counts (the input ring refills on odd and even tokens)."""
     bs, H = 10, 8
     pr, x, dt, B, C = _tokens_problem(bs, T, H=H, N=N, seed=T + N)
     aligned_pool, aligned_out, aligned_inter = _run(op, pr, x, dt, B, C)
