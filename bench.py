@@ -1013,12 +1013,13 @@ def run_copy(args) -> None:
 
 
 def bytes_per_call_tokens(bs: int, T: int, intermediate: bool, H: int = NHEADS,
-                          P: int = HEADDIM, N: int = DSTATE, G: int = NGROUPS) -> int:
+                          P: int = HEADDIM, N: int = DSTATE, G: int = NGROUPS,
+                          state_bytes: int = 4) -> int:
     """Algorithmic bytes of one multi-token call: the state read and written once, T tokens of
     inputs and outputs, and (optionally) T intermediate states written."""
-    state = 2 * bs * H * P * N * 4
+    state = 2 * bs * H * P * N * state_bytes
     per_token = bs * H * P * 2 * 2 + 2 * bs * G * N * 2 + bs * H * 2
-    inter = T * bs * H * P * N * 4 if intermediate else 0
+    inter = T * bs * H * P * N * state_bytes if intermediate else 0
     return state + T * per_token + bs * 4 + 3 * H * 4 + inter
 
 
@@ -1049,13 +1050,18 @@ def run_tokens(args) -> None:
     handle = ssu.ssu_create(0)
     ssu.ssu_set_pdl(handle, not args.no_pdl)
     bs, H = args.batch, NHEADS
-    w = Workload(bs, H, dev, seed=5, l2_bytes=l2)
+    N, sdt = args.dstate, args.state_dtype
+    eb = 2 if sdt == "bf16" else 4
+    w = Workload(bs, H, dev, seed=5, l2_bytes=l2, N=N, state_dtype=sdt)
     rng = np.random.default_rng(9)
     peaks = load_peaks()
     shapes = [None]
     tokens_list = tuple(args.tokens_list)
     if args.sweep:
-        shapes = [(r, w) for r in (4, 8, 16) for w in (1, 2, 4)]
+        rpi = max(1, 512 // (N * eb))
+        nc = (8 if sdt == "bf16" else 4) * max(1, N * eb // 512)
+        ks = (2, 4, 8, 16) if (N == DSTATE and sdt == "f32") else (2, 4, 8)
+        shapes = [(k * rpi, w) for k in ks if k * nc <= 64 for w in (1, 2, 4)]
         tokens_list = (2, 4)
     cpu_by_t = {}
     for T in tokens_list:
@@ -1063,7 +1069,7 @@ def run_tokens(args) -> None:
             (w.n_sets, bs, T, H, HEADDIM), dtype=np.float32)).view(np.int16)).view(
             torch.bfloat16).to(dev)
         bc = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(
-            (w.n_sets, 2, bs, T, 1, DSTATE), dtype=np.float32)).view(np.int16)).view(
+            (w.n_sets, 2, bs, T, 1, N), dtype=np.float32)).view(np.int16)).view(
             torch.bfloat16).to(dev)
         dt = torch.from_numpy(wl.f32_to_bf16_bits(rng.uniform(
             -4, 0, (w.n_sets, bs, T, H)).astype(np.float32)).view(np.int16)).view(
@@ -1075,7 +1081,9 @@ def run_tokens(args) -> None:
                 ssu.ssu_set_launch(handle, ssu.SSU_MODE_AUTO)
             else:
                 ssu.ssu_set_launch(handle, ssu.SSU_MODE_VEC, shape[0], shape[1])
-            inter = (torch.empty(bs, T, H, HEADDIM, DSTATE, device=dev) if with_inter else None)
+            inter = (torch.empty(bs, T, H, HEADDIM, N, device=dev,
+                                 dtype=torch.bfloat16 if sdt == "bf16" else torch.float32)
+                     if with_inter else None)
 
             def call(i, stream_ptr, T=T, x=x, bc=bc, dt=dt, out=out, inter=inter):
                 k = i % w.n_sets
@@ -1085,23 +1093,25 @@ def run_tokens(args) -> None:
             n = max(w.n_sets * 4, 400)
             us = graph_time_us(lambda i: call(i, torch.cuda.current_stream().cuda_stream),
                                w.n_sets, calls=n)
-            moved = bytes_per_call_tokens(bs, T, with_inter)
+            moved = bytes_per_call_tokens(bs, T, with_inter, N=N, state_bytes=eb)
             gbs = moved / (us * 1e-6) / 1e9
-            rec = {"tokens": T, "batch": bs, "intermediate": with_inter,
+            rec = {"tokens": T, "batch": bs, "intermediate": with_inter, "dstate": N,
+                   "state_dtype": sdt,
                    "launch": list(shape) if shape else "table",
                    "programmatic_dependent_launch": not args.no_pdl,
                    "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
                    "gbs": round(gbs, 1),
                    "frac_of_measured_peak": round(gbs / peaks["hbm_gbs"], 4)}
             if shape is None:
-                tag = f"tokens{T}-batch{bs}" + ("-inter" if with_inter else "")
+                tag = f"tokens{T}-batch{bs}" + ("-inter" if with_inter else "") + (
+                    "" if (N == DSTATE and sdt == "f32") else f"-n{N}-{sdt}")
                 rec["roofline"] = {
                     "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                     "traffic": recorded_traffic(tag, sources=TOKENS_SOURCES),
                     "algorithmic_bytes_per_launch": moved, "peak_source": peaks["source"],
                     "kernel": "ssu_tokens_kernel"}
-                if not args.skip_cpu:
+                if not args.skip_cpu and N == DSTATE and sdt == "f32":
                     if T not in cpu_by_t:
                         cpu_by_t[T] = cpu_baseline_tokens(bs, H, T)
                     rec["cpu_baseline"] = cpu_by_t[T]

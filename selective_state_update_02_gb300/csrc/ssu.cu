@@ -85,29 +85,38 @@ ssu_status_t parse_launch_spec(const char *spec, ssu_launch_t *out) {
 namespace {
 
 // Built-in launch-shape table, from the cold-L2 sweeps on GB300 (bench.py --sweep with and
-// without --dstate / --state-dtype, batch 1 to 512, 16 heads, headdim 64), keyed by the bytes
-// of one state row.  A warp's unit of work is a "slot": the rows one 16-byte vector
-// instruction covers (512 bytes: 1 row of 512 B, 2 of 256 B, 4 of 128 B; a 1 KiB row takes two
-// vectors per lane).  A small call gives each warp 2 slots in CTAs of 4 warps; from a size on,
-// 8 slots per warp (4 rows of 1 KiB), in CTAs of 4 warps (2 for a bf16 state of 512 B rows and
-// for 1 KiB rows).  The size is counted in state bytes per call, for 152 SMs: 8 MiB (batch 16
-// at 16 heads of 64 rows of 512 B; 16 MiB for 1 KiB rows).  16 rows per warp is slower in every bucket.  The tile
-// never exceeds the headdim.
+// without --dstate / --state-dtype, batch 8, 128 and 512 at 16 heads, headdim 64), keyed by
+// the bytes of one state row.  A warp's unit of work is a vector row ("slot"): the rows one
+// 16-byte-per-lane instruction covers (1 row of 512 B, 2 of 256 B, 4 of 128 B; a 1 KiB row
+// takes two vectors per lane).  Call sizes are state bytes per call, scaled to 152 SMs.
+//   1 KiB rows:  4 slots x 2 warps from 16 MiB, else 2 x 4.
+//   512 B rows:  8 slots x 4 warps (x 2 for bf16) from 8 MiB (batch 16 at 16 heads of 64 rows),
+//                else 2 x 4.  16 rows per warp is slower in every bucket.
+//   256 B rows:  8 slots x 4 warps from 8 MiB, else 4 x 4 (fp32 dstate 64, batch 8: 3.14 us at
+//                2 slots, 2.62 at 4).
+//   128 B rows:  8 slots x 2 warps from 32 MiB, 4 x 4 from 8 MiB (batch 128: 8.19 us at 8 x 2,
+//                7.84 at 4 x 4), else 2 x 8.
+// The tile never exceeds the headdim.
 ssu_launch_t table_launch(const ssu_handle_s &hd, const ssu_shape_t &s, const ssu_strides_t *st) {
     (void)st;
     const bool bf16 = s.state_dtype == SSU_STATE_BF16;
     const long long row_bytes = s.dstate * (bf16 ? 2 : 4);
     const int rpi = ssu_host::rows_per_instruction(s.dstate, s.state_dtype);
     const long long bytes = s.batch * s.nheads * s.headdim * row_bytes;
-    const long long large_from = row_bytes >= 1024 ? (16LL << 20) : (8LL << 20);
-    const bool large = bytes * 152 >= large_from * hd.sm_count;
+    auto at_least = [&](long long mib) { return bytes * 152 >= (mib << 20) * hd.sm_count; };
     int slots, wpc;
     if (row_bytes >= 1024) {
-        slots = large ? 4 : 2;
-        wpc = large ? 2 : 4;
+        slots = at_least(16) ? 4 : 2;
+        wpc = at_least(16) ? 2 : 4;
+    } else if (row_bytes == 512) {
+        slots = at_least(8) ? 8 : 2;
+        wpc = at_least(8) && bf16 ? 2 : 4;
+    } else if (row_bytes == 256) {
+        slots = at_least(8) ? 8 : 4;
+        wpc = 4;
     } else {
-        slots = large ? 8 : 2;
-        wpc = large && bf16 && row_bytes >= 512 ? 2 : 4;
+        slots = at_least(32) ? 8 : at_least(8) ? 4 : 2;
+        wpc = at_least(32) ? 2 : at_least(8) ? 4 : 8;
     }
     int rpw = slots * rpi;
     while (slots > 1 && rpw > s.headdim) {

@@ -50,26 +50,6 @@ __host__ __device__ __forceinline__ int group_of(int h, unsigned long long m) {
     return static_cast<int>((static_cast<unsigned long long>(h) * m) >> 32);
 }
 
-// floor(n / d) for 0 <= n < 2^31 and 1 <= d < 2^31 by a multiply and a shift.  With
-// l = ceil(log2 d) and m = floor(2^(31+l) / d) + 1:  2^(31+l) < m d <= 2^(31+l) + d <=
-// 2^(31+l) + 2^l, and for such m, floor(n m / 2^(31+l)) = floor(n / d) for every n < 2^31
-// (Granlund and Montgomery, "Division by invariant integers using multiplication", 1994,
-// Theorem 4.2 with N = 31).  m <= 2^32 + 1, so n m < 2^64 needs no wider product.
-struct FastDiv {
-    unsigned long long m;
-    unsigned shift;
-};
-
-__host__ __device__ inline FastDiv fast_div(unsigned d) {
-    unsigned l = 0;
-    while ((1ull << l) < d) ++l;
-    return FastDiv{(1ull << (31 + l)) / d + 1, 31 + l};
-}
-
-__host__ __device__ __forceinline__ unsigned fast_div_apply(unsigned n, FastDiv f) {
-    return static_cast<unsigned>((static_cast<unsigned long long>(n) * f.m) >> f.shift);
-}
-
 __device__ __forceinline__ float softplus_f32(float z) {
     // log(1 + e^z); above 20 the correction is below fp32 resolution of z.
     return z > 20.0f ? z : log1pf(expf(z));

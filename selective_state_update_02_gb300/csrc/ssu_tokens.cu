@@ -91,18 +91,22 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
         return ssu_update(handle, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
                           out, shape, strides, stream);
     const ssu_shape_t &s = *shape;
-    // 32 fp32 state values per lane: 8 vector rows at 4 columns per lane (fp32 at dstate 64
-    // and 128), 4 at 8 columns (dstate 256, a bf16 state); one warp per CTA.  Fewer rows for a
-    // small headdim.  The handle's VEC override (for sweeps) sets rows per warp and warps per
-    // CTA instead.
+    // From the sweeps (bench.py --tokens --sweep, batch 128, T = 2 and 4, every bucket): an fp32
+    // state takes 32 fp32 values per lane (8 vector rows at 4 columns per lane, 4 at 8 for
+    // dstate 256), a bf16 state 64 (8 vector rows at 8 columns: 2, 4 or 8 rows per vector
+    // row), in CTAs of 2 warps; bf16 dstate 128 at T = 2 / 4: 19.45 / 25.52 us with 4 vector
+    // rows, 16.16 / 20.67 with 8; fp32 dstate 128: 24.30 / 29.33 at 1 warp per CTA, 23.87 /
+    // 29.14 at 2.  Fewer rows for a small headdim.  The handle's VEC override (for sweeps) sets
+    // rows per warp and warps per CTA instead.
     const int rpi = ssu_host::rows_per_instruction(s.dstate, s.state_dtype);
     const long long row_bytes = s.dstate * (s.state_dtype == SSU_STATE_BF16 ? 2 : 4);
     const int vpr = row_bytes >= 512 ? static_cast<int>(row_bytes / 512) : 1;  // vectors per lane
     const int nc = (s.state_dtype == SSU_STATE_BF16 ? 8 : 4) * vpr;            // columns per lane
-    int slots = 32 / nc;
+    int slots = (s.state_dtype == SSU_STATE_BF16 ? 64 : 32) / nc;
     while (slots > 1 && slots * rpi > s.headdim) slots >>= 1;
     int rpw = slots * rpi;
-    int wpc = 1;
+    int wpc = 2;
+    while (wpc > 1 && rpw * wpc > s.headdim) wpc >>= 1;
     if (handle->has_override && handle->override_launch.mode == SSU_MODE_VEC) {
         rpw = handle->override_launch.rows_per_warp;
         wpc = handle->override_launch.warps_per_cta;

@@ -228,9 +228,10 @@ __device__ __forceinline__ void token_loop(
 }
 
 // Registers per thread: 96 for a tile of at most 32 fp32 state values per lane, so 20 warps
-// fit on an SM (5 per sub-partition's register file); the ring of 2 tokens then needs no
-// spill at 4 columns per lane, the ring of 1 none at 8 (ptxas, CUDA 13.0).  Larger tiles take
-// 128.
+// fit on an SM (5 per sub-partition's register file): fp32 dstate 128 at 8 rows spills 8
+// bytes there (ptxas, CUDA 13.0) and still ran faster than at 104 registers without a spill
+// (T = 3 / 4 / 8: 26.6 / 29.4 / 40.2 against 27.5 / 31.3 / 43.4 us).  Larger tiles (a bf16
+// state's 64 values) take 128, where they need no spill.
 template <int RPW, int N, typename ST>
 constexpr int tokens_max_regs() {
     using G = RowGeo<N, ST>;

@@ -54,24 +54,34 @@ __device__ __forceinline__ float update_row(float (&v)[RowGeo<N, ST>::NC], float
         return update_lane_scalar<NC>(v, dA, k, bb, cc);
 }
 
-// Registers per thread for an instantiation: the smallest multiple of 8 at which ptxas
-// (CUDA 13.0, sm_103a) keeps every variable in registers, from -Xptxas -v at each cap.  Left
-// to itself the compiler takes far more for some (fp32 dstate 64 with 16 rows per warp: 118;
-// bf16 with 8 vector rows: 103-108; fp32 dstate 256 with 4 rows: 115), which costs resident
-// warps.  At most 128, so a CTA of 16 warps always fits.
+// Registers per thread for an instantiation.  Under the launch bound of a 16-warp CTA alone
+// the compiler takes far more than it needs for some (fp32 dstate 64 with 16 rows per warp:
+// 118; bf16 with 8 vector rows: 103-108; dstate 256 with 4 vector rows: 115-117; fp32 dstate
+// 128 with 16 rows: 128 and a spill), which costs resident warps; those are compiled as
+// ssu_vec_kernel_capped, held to the smallest multiple of 8 at which ptxas (CUDA 13.0,
+// sm_103a) keeps every variable in registers (fp32 dstate 128 at 8 rows: 74 -> 64, the 32
+// warps per SM its timing rests on).  The others (128 here) keep the launch bound only: a
+// register cap they do not need changed their schedules (fp32 dstate 128 with 2 rows per
+// warp: 40 -> 44 registers under a cap of 64, batch 8 at 3.84 instead of 3.38 us).
 template <int RPW, int N, typename ST>
 constexpr int vec_max_regs() {
     using G = RowGeo<N, ST>;
     constexpr int S = RPW / G::RPI, V = S * G::VPR;  // 16-byte vectors of state per lane
-    if constexpr (sizeof(ST) == 4) return V <= 8 ? (G::VPR == 2 && V == 8 ? 72 : 64) : 104;
-    return S <= 2 ? 64 : S <= 4 ? 72 : 96;
+    if constexpr (sizeof(ST) == 4) {
+        if (V >= 16) return 104;            // fp32 dstate 128 at 16 rows, dstate 256 at 8
+        if (V == 8) return G::VPR == 2 ? 72 : 64;
+        return 128;
+    }
+    if (S >= 8) return 96;
+    if (S == 4) return 72;
+    return 128;
 }
 
-// Grid: x = slab of rows, y = head, z = request (requests beyond gridDim.z loop), so the
-// slot lookup at the head of the dependency chain needs no index arithmetic.
+// The decode step of one CTA.  Grid: x = slab of rows, y = head, z = request (requests beyond
+// gridDim.z loop), so the slot lookup at the head of the dependency chain needs no index
+// arithmetic.
 template <int RPW, int N, typename ST, bool kIdx64>
-__global__ void __maxnreg__((vec_max_regs<RPW, N, ST>()))
-    ssu_vec_kernel(const __grid_constant__ SsuParams p) {
+__device__ __forceinline__ void vec_step(const SsuParams &p) {
     using G = RowGeo<N, ST>;
     using F = VecForm<RPW, N, ST>;
     constexpr int S = F::S, NC = G::NC, RPI = G::RPI;
@@ -179,6 +189,18 @@ __global__ void __maxnreg__((vec_max_regs<RPW, N, ST>()))
     pdl_trigger();  // this CTA's stores are issued: a dependent launch may start its CTAs
 }
 
+template <int RPW, int N, typename ST, bool kIdx64>
+__global__ void __launch_bounds__(32 * kMaxWarpsPerCta)
+    ssu_vec_kernel(const __grid_constant__ SsuParams p) {
+    vec_step<RPW, N, ST, kIdx64>(p);
+}
+
+template <int RPW, int N, typename ST, bool kIdx64>
+__global__ void __maxnreg__((vec_max_regs<RPW, N, ST>()))
+    ssu_vec_kernel_capped(const __grid_constant__ SsuParams p) {
+    vec_step<RPW, N, ST, kIdx64>(p);
+}
+
 // Launches one instantiation; with `pdl` the launch may begin before the previous kernel in
 // the stream has finished (the kernel waits for it before touching memory).
 template <int RPW, int N, typename ST, bool kIdx64>
@@ -192,7 +214,10 @@ cudaError_t launch_vec_one(const SsuParams &p, dim3 grid, dim3 block, bool pdl, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, ssu_vec_kernel<RPW, N, ST, kIdx64>, p);
+    if constexpr (vec_max_regs<RPW, N, ST>() < 128)
+        return cudaLaunchKernelEx(&cfg, ssu_vec_kernel_capped<RPW, N, ST, kIdx64>, p);
+    else
+        return cudaLaunchKernelEx(&cfg, ssu_vec_kernel<RPW, N, ST, kIdx64>, p);
 }
 
 // Rows per warp this build instantiates for a (dstate, state type): RPI x {1, 2, 4, 8}, and 16

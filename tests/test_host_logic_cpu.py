@@ -38,15 +38,3 @@ def test_group_index_without_division(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
 
-
-def test_tile_number_division(tmp_path):
-    """fast_div_apply(n, fast_div(d)) == n // d for n < 2^31 at the multiples of every d up to
-    70000, around powers of two up to 2^31, and at random pairs (tests/c/fast_div.cu)."""
-    from selective_state_update_02_gb300 import _build
-    nvcc = _build.nvcc_path()
-    exe = tmp_path / "fast_div"
-    subprocess.run([nvcc, *_build.ARCH, "-O2", "-std=c++17",
-                    "-I", str(ROOT / "selective_state_update_02_gb300" / "csrc"),
-                    str(ROOT / "tests" / "c" / "fast_div.cu"), "-o", str(exe)], check=True)
-    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
-    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
