@@ -48,10 +48,25 @@ PAGE_US = {8: 4.02, 128: 24.1, 512: 85.7}   # sglang PR #41223 Speedup Result, B
 CSRC = ROOT / "selective_state_update_02_gb300" / "csrc"
 KERNEL_SOURCES = [CSRC / "ssu_vec.cuh", CSRC / "ssu_device.cuh"]     # VEC kernel
 TOKENS_SOURCES = [CSRC / "ssu_tokens.cuh", CSRC / "ssu_device.cuh"]  # multi-token kernel
+MMA_SOURCES = [CSRC / "ssu_tokens_mma.cuh", CSRC / "ssu_tokens.cuh",  # chunked multi-token
+               CSRC / "ssu_device.cuh"]
 COPY_SOURCES = [CSRC / "ssu_copy.cu", CSRC / "ssu_device.cuh"]       # block-copy kernels
 
 
 # ---- arithmetic of the measurement (host logic, tested on CPU) ---------------------------
+
+
+def tokens_kernel(T: int, with_inter: bool, N: int, state_dtype: str, forced: bool) -> str:
+    """The kernel the library's ssu_update_tokens picks for the bench's aligned operands (the
+    rule of mma_min_tokens in ssu_tokens.cu): the chunked one without intermediate states and
+    without a forced launch shape, for an fp32 state (dstate 64 or 128) from 5 tokens and a
+    bf16 state of dstate 128 from 16; else the general one.  Names the roofline's kernel."""
+    if with_inter or forced or N not in (64, 128):
+        return "ssu_tokens_kernel"
+    if state_dtype == "f32":
+        return "ssu_tokens_mma_kernel" if T >= 5 else "ssu_tokens_kernel"
+    return "ssu_tokens_mma_kernel" if (N == 128 and T >= 16) else "ssu_tokens_kernel"
+
 
 def bytes_per_call(bs: int, H: int = NHEADS, P: int = HEADDIM, N: int = DSTATE,
                    G: int = NGROUPS, idx_bytes: int = 4, state_bytes: int = 4) -> int:
@@ -1062,7 +1077,8 @@ def run_tokens(args) -> None:
         nc = (8 if sdt == "bf16" else 4) * max(1, N * eb // 512)
         ks = (2, 4, 8, 16) if (N == DSTATE and sdt == "f32") else (2, 4, 8)
         shapes = [(k * rpi, w) for k in ks if k * nc <= 64 for w in (1, 2, 4)]
-        tokens_list = (2, 4)
+        if tokens_list == (1, 2, 3, 4):  # the default list: sweep at 2 and 4 tokens
+            tokens_list = (2, 4)
     cpu_by_t = {}
     for T in tokens_list:
         x = torch.from_numpy(wl.f32_to_bf16_bits(rng.standard_normal(
@@ -1078,7 +1094,7 @@ def run_tokens(args) -> None:
         for shape, with_inter in [(sh, wi) for sh in shapes
                                   for wi in ((False,) if args.sweep else (False, True))]:
             if shape is None:
-                ssu.ssu_set_launch(handle, ssu.SSU_MODE_AUTO)
+                ssu.ssu_set_launch_override(handle, args.launch or "auto")
             else:
                 ssu.ssu_set_launch(handle, ssu.SSU_MODE_VEC, shape[0], shape[1])
             inter = (torch.empty(bs, T, H, HEADDIM, N, device=dev,
@@ -1097,7 +1113,7 @@ def run_tokens(args) -> None:
             gbs = moved / (us * 1e-6) / 1e9
             rec = {"tokens": T, "batch": bs, "intermediate": with_inter, "dstate": N,
                    "state_dtype": sdt,
-                   "launch": list(shape) if shape else "table",
+                   "launch": list(shape) if shape else (args.launch or "table"),
                    "programmatic_dependent_launch": not args.no_pdl,
                    "us_per_call": round(us, 3), "us_per_token": round(us / T, 3),
                    "gbs": round(gbs, 1),
@@ -1105,12 +1121,15 @@ def run_tokens(args) -> None:
             if shape is None:
                 tag = f"tokens{T}-batch{bs}" + ("-inter" if with_inter else "") + (
                     "" if (N == DSTATE and sdt == "f32") else f"-n{N}-{sdt}")
+                kern = tokens_kernel(T, with_inter, N, sdt, bool(args.launch))
                 rec["roofline"] = {
                     "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                    "traffic": recorded_traffic(tag, sources=TOKENS_SOURCES),
+                    "traffic": recorded_traffic(
+                        tag, sources=MMA_SOURCES if kern == "ssu_tokens_mma_kernel"
+                        else TOKENS_SOURCES),
                     "algorithmic_bytes_per_launch": moved, "peak_source": peaks["source"],
-                    "kernel": "ssu_tokens_kernel"}
+                    "kernel": kern}
                 if not args.skip_cpu and N == DSTATE and sdt == "f32":
                     if T not in cpu_by_t:
                         cpu_by_t[T] = cpu_baseline_tokens(bs, H, T)

@@ -15,7 +15,7 @@ SOURCES = [CSRC / "ssu.cu", CSRC / "ssu_tokens.cu", CSRC / "ssu_copy.cu",
            CSRC / "ssu_host.cpp"]
 HEADERS = [ROOT / "include" / "ssu.h", CSRC / "ssu_device.cuh", CSRC / "ssu_host.h",
            CSRC / "ssu_vec.cuh", CSRC / "ssu_stage.cuh",
-           CSRC / "ssu_tokens.cuh"]
+           CSRC / "ssu_tokens.cuh", CSRC / "ssu_tokens_mma.cuh"]
 OBJDIR = PKG / "_build"
 LIB = PKG / "libssu.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -10,6 +10,7 @@
 #include "ssu.h"
 #include "ssu_host.h"
 #include "ssu_tokens.cuh"
+#include "ssu_tokens_mma.cuh"
 
 using ssu_host::aligned;
 using ssu_host::DeviceGuard;
@@ -52,6 +53,53 @@ cudaError_t launch_tokens(const TokenParams &q, dim3 grid, int dstate, bool bf16
     return cudaErrorInvalidValue;
 }
 
+// The chunked kernel's instantiations: fp32 state at dstate 64 and 128, bf16 at 128 (a bf16
+// state at dstate 64 never takes it, see mma_min_tokens).
+cudaError_t launch_mma(const TokenParams &q, dim3 grid, int dstate, bool bf16, bool i64,
+                       int warps, bool pdl, cudaStream_t st) {
+    if (bf16) {
+        if (dstate != 128) return cudaErrorInvalidValue;
+        return i64 ? launch_tokens_mma<128, __nv_bfloat16, true>(q, grid, warps, pdl, st)
+                   : launch_tokens_mma<128, __nv_bfloat16, false>(q, grid, warps, pdl, st);
+    }
+    if (dstate == 64)
+        return i64 ? launch_tokens_mma<64, float, true>(q, grid, warps, pdl, st)
+                   : launch_tokens_mma<64, float, false>(q, grid, warps, pdl, st);
+    if (dstate == 128)
+        return i64 ? launch_tokens_mma<128, float, true>(q, grid, warps, pdl, st)
+                   : launch_tokens_mma<128, float, false>(q, grid, warps, pdl, st);
+    return cudaErrorInvalidValue;
+}
+
+// The chunked matrix-form kernel (ssu_tokens_mma.cuh) takes a call without intermediate
+// states and without a launch override when dstate is 64 or 128, headdim is a multiple of 8,
+// B, C and x can be staged in 16-byte pieces (base addresses 16-byte aligned, every stride a
+// multiple of 8 elements) and the call has at least mma_min_tokens tokens.  Its work per tile
+// hardly depends on T (up to 8 tokens per chunk), the general kernel's grows with T; the
+// crossovers measured at batch 128, 16 heads (us per call, general / chunked):
+//   fp32 dstate 128: T 4: 28.7 / 29.3, T 6: 35.1 / 30.6, T 8: 40.2 / 31.5, T 16: 63.6 / 43.9
+//   fp32 dstate 64:  T 4: 15.7 / 17.7, T 6: 18.9 / 18.2, T 8: 22.5 / 18.6, T 16: 35.8 / 27.4
+//   bf16 dstate 128: T 4: 20.3 / 29.1, T 8: 30.5 / 31.5, T 16: 49.2 / 46.6
+//   bf16 dstate 64:  T 4: 12.6 / 17.8, T 8: 18.3 / 20.1, T 16: 28.1 / 30.2
+// (a bf16 state halves the general kernel's bytes, not the chunked kernel's arithmetic).
+int mma_min_tokens(int64_t dstate, int32_t state_dtype) {
+    if (state_dtype != SSU_STATE_BF16) return 5;
+    return dstate == 128 ? 16 : SSU_MAX_TOKENS + 1;
+}
+
+bool mma_eligible(const ssu_shape_t &s, const ssu_strides_t &str, const ssu_token_strides_t &ts,
+                  const void *x, const void *B, const void *C, int64_t tokens) {
+    if (s.dstate != 64 && s.dstate != 128) return false;
+    if (tokens < mma_min_tokens(s.dstate, s.state_dtype)) return false;
+    if (s.headdim % 8 != 0) return false;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16)) return false;
+    const long long strides[] = {str.x[0], str.x[1], ts.x, str.B[0], str.B[1], ts.B,
+                                 str.C[0], str.C[1], ts.C};
+    for (long long v : strides)
+        if (v % 8 != 0) return false;
+    return true;
+}
+
 }  // namespace
 
 extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
@@ -91,6 +139,8 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
         return ssu_update(handle, state_pool, state_batch_indices, x, dt, dt_bias, A, B, C, D,
                           out, shape, strides, stream);
     const ssu_shape_t &s = *shape;
+    const bool use_mma = !intermediate && !handle->has_override &&
+                         mma_eligible(s, *strides, *ts, x, B, C, tokens);
     // From the sweeps (bench.py --tokens --sweep, batch 128, T = 2 and 4, every bucket): an fp32
     // state takes 32 fp32 values per lane (8 vector rows at 4 columns per lane, 4 at 8 for
     // dstate 256), a bf16 state 64 (8 vector rows at 8 columns: 2, 4 or 8 rows per vector
@@ -117,6 +167,11 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
             return fail(SSU_ERR_UNSUPPORTED,
                         "the multi-token kernel holds at most 64 state values per lane (32 in "
                         "CTAs of more than 4 warps)");
+    }
+    if (use_mma) {  // 16 rows per warp, up to 4 warps (64 rows) per CTA
+        rpw = kMmaRowsPerWarp;
+        wpc = kMmaWarpsPerCta;
+        while (wpc > 1 && rpw * (wpc / 2) >= s.headdim) wpc >>= 1;
     }
     const long long slabs = (s.headdim + rpw * wpc - 1) / (rpw * wpc);
     const long long tiles = s.batch * s.nheads * slabs;
@@ -190,8 +245,10 @@ extern "C" ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
     const bool bf16 = s.state_dtype == SSU_STATE_BF16, i64 = s.index_dtype == SSU_INDEX_I64;
     const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(s.nheads),
                     static_cast<unsigned>(s.batch < 65535 ? s.batch : 65535));
-    const cudaError_t e = launch_tokens(q, grid, static_cast<int>(s.dstate), bf16, i64, rpw,
-                                        wpc, handle->pdl, cs);
+    const cudaError_t e =
+        use_mma ? launch_mma(q, grid, static_cast<int>(s.dstate), bf16, i64, wpc, handle->pdl, cs)
+                : launch_tokens(q, grid, static_cast<int>(s.dstate), bf16, i64, rpw, wpc,
+                                handle->pdl, cs);
     if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
     return ok();
 }

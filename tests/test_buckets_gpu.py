@@ -108,8 +108,8 @@ def test_rows_per_warp_outside_the_bucket_are_refused(op, N, dtype):
 
 @pytest.mark.parametrize("N,dtype", COMBOS + [(128, "f32")])
 def test_every_token_shape_is_bitwise_identical(op, N, dtype):
-    # The multi-token kernel's tiles (rows per warp, warps per CTA) change which warp updates
-    # which rows, never the arithmetic: every shape gives the bits of the table's shape.
+    # The general multi-token kernel's tiles (rows per warp, warps per CTA) change which warp
+    # updates which rows, never the arithmetic: every shape gives the same bits.
     bs, T, H, P = 9, 3, 8, 40
     pr = wl.make_problem(bs, H, P=P, N=N, pool_size=12, seed=19, state_dtype=dtype)
     rng = np.random.default_rng(20)
@@ -125,10 +125,13 @@ def test_every_token_shape_is_bitwise_identical(op, N, dtype):
         return dev["state_pool"].view(torch.int16).clone() if dtype == "bf16" else \
             dev["state_pool"].clone(), out.view(torch.int16).clone()
 
-    ref_pool, ref_out = run()
     rpi = rows_per_instruction(N, dtype)
     nc = 8 if (dtype == "bf16" or N == 256) else 4
     try:
+        # the reference: one slot per lane, one warp per CTA (a forced shape runs the general
+        # kernel; without one, dstate 64 and 128 run the chunked kernel, which sums otherwise)
+        op.set_launch(ssu.SSU_MODE_VEC, rpi, 1)
+        ref_pool, ref_out = run()
         for slots in (1, 2, 4, 8):
             if slots * nc > 32:
                 continue
@@ -155,15 +158,20 @@ def test_skipped_requests(op, N, dtype):
 
 
 @pytest.mark.parametrize("N,dtype", COMBOS + [(128, "f32")])
-def test_tokens(op, N, dtype):
-    bs, T, H, P = 7, 3, 8, 40
+@pytest.mark.parametrize("with_inter,T", [(True, 5), (False, 5), (False, 16)],
+                         ids=["inter", "no_inter", "no_inter-16"])
+def test_tokens(op, N, dtype, with_inter, T):
+    # with intermediate states the general kernel runs; without them, the chunked kernel for
+    # an fp32 state from 5 tokens and a bf16 state of dstate 128 from 16
+    bs, H, P = 7, 8, 40
     pr = wl.make_problem(bs, H, P=P, N=N, pool_size=12, seed=11, state_dtype=dtype)
     rng = np.random.default_rng(12)
     steps = [wl.request_inputs(rng, bs, H, P, N) for _ in range(T)]
     x, dt, B, C = (np.stack([s[k] for s in steps], 1) for k in range(4))
     dev = to_device(pr)
     out = torch.zeros(bs, T, H, P, dtype=torch.bfloat16, device="cuda")
-    inter = torch.zeros(bs, T, H, P, N, dtype=dev["state_pool"].dtype, device="cuda")
+    inter = (torch.zeros(bs, T, H, P, N, dtype=dev["state_pool"].dtype, device="cuda")
+             if with_inter else None)
     op.tokens(dev["state_pool"], dev["state_batch_indices"], bf16_tensor(x, "cuda"),
               bf16_tensor(dt, "cuda"), dev["dt_bias"], dev["A"], bf16_tensor(B, "cuda"),
               bf16_tensor(C, "cuda"), dev["D"], out, inter)
@@ -172,10 +180,12 @@ def test_tokens(op, N, dtype):
                                                      pr.A, B, C, pr.D)
     got = pool_host(dev["state_pool"])
     check_state(got[pr.idx], ref_pool[pr.idx])
-    got_inter = pool_host(inter.view(bs, T * H, P, N)).reshape(bs, T, H, P, N)
+    got_inter = (pool_host(inter.view(bs, T * H, P, N)).reshape(bs, T, H, P, N)
+                 if with_inter else None)
     outb = bits_of(out)
     for t in range(T):
-        check_state(got_inter[:, t], ref_inter[:, t], f"intermediate {t}")
+        if with_inter:
+            check_state(got_inter[:, t], ref_inter[:, t], f"intermediate {t}")
         Ch, Dx = expected_terms(x[:, t], pr.D, C[:, t], 1, H)
         check_y(outb[:, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, N, f"y token {t}")
 

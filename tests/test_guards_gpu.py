@@ -81,8 +81,12 @@ def test_decode_step_writes_nothing_outside_its_buffers(op, N, dtype):
     assert _same(pool.t, ref["state_pool"]) and _same(out.t, ref["out"])
 
 
-@pytest.mark.parametrize("N,dtype,T", [(128, "f32", 3), (64, "bf16", 2), (256, "f32", 5)])
-def test_multi_token_step_writes_nothing_outside_its_buffers(op, N, dtype, T):
+@pytest.mark.parametrize("N,dtype,T", [(128, "f32", 3), (64, "bf16", 2), (256, "f32", 5),
+                                       (128, "f32", 11), (64, "f32", 9), (128, "bf16", 17)])
+@pytest.mark.parametrize("with_inter", [True, False], ids=["inter", "no_inter"])
+def test_multi_token_step_writes_nothing_outside_its_buffers(op, N, dtype, T, with_inter):
+    # without intermediate states the longer calls at dstate 64 and 128 run the chunked kernel
+    # (headdim 40 is a multiple of 8), whose warps stage their inputs in chunks of 8 tokens
     bs, H, P, G = 10, 8, 40, 2
     pr = _problem(bs, H, P, N, G, 16, dtype, seed=T + N)
     rng = np.random.default_rng(T)
@@ -103,7 +107,7 @@ def test_multi_token_step_writes_nothing_outside_its_buffers(op, N, dtype, T):
         else:
             pool = dev["state_pool"]
         op.tokens(pool, dev["state_batch_indices"], x, dt, dev["dt_bias"], dev["A"], B, C,
-                  dev["D"], out, inter)
+                  dev["D"], out, inter if with_inter else None)
         assert op.get_error() == (2, 2)
         results.append((pool, out, inter))
     assert gp.intact() and go.intact() and gi.intact()

@@ -44,6 +44,14 @@ TOKENS_TABLE = {           # the multi-token table's tiles: (cap, spill bytes al
     (8, 256, "bf16"): (128, 0),
 }
 
+# The chunked multi-token kernel (dstate -> (cap, spill bytes allowed)): 4 CTAs of 4 warps per
+# SM at 128 registers; the state takes 64 of them at dstate 128.
+MMA_TABLE = {
+    (128, "f32"): (128, 0),
+    (128, "bf16"): (128, 8),
+    (64, "f32"): (128, 0),
+}
+
 
 def _ptxas_report(tmp_path: Path, unit: str) -> dict:
     from selective_state_update_02_gb300 import _build
@@ -57,11 +65,16 @@ def _ptxas_report(tmp_path: Path, unit: str) -> dict:
         name = block.split("'")[0]
         m = re.search(r"(ssu_vec_kernel|ssu_tokens_kernel)(?:_capped)?ILi(\d+)ELi(\d+)E(\w+?)"
                       r"Lb([01])E", name)
+        mm = re.search(r"ssu_tokens_mma_kernelILi(\d+)E(\w+?)Lb([01])E", name)
         regs = re.search(r"Used (\d+) registers", block)
         spill = re.search(r"(\d+) bytes spill stores", block)
         if m and regs and spill:
             st = "bf16" if "nv_bfloat16" in m.group(4) else "f32"
             key = (m.group(1), int(m.group(2)), int(m.group(3)), st, m.group(5) == "1")
+            kernels[key] = (int(regs.group(1)), int(spill.group(1)))
+        elif mm and regs and spill:
+            st = "bf16" if "nv_bfloat16" in mm.group(2) else "f32"
+            key = ("ssu_tokens_mma_kernel", int(mm.group(1)), st, mm.group(3) == "1")
             kernels[key] = (int(regs.group(1)), int(spill.group(1)))
     return kernels
 
@@ -76,6 +89,17 @@ def test_table_kernels_fit_their_registers(tmp_path, unit, kernel, table):
         cap, spill_ok = budget if isinstance(budget, tuple) else (budget, 0)
         for i64 in (False, True):
             key = (kernel, rpw, n, st, i64)
+            assert key in report, f"{key} not compiled"
+            regs, spill = report[key]
+            assert spill <= spill_ok, f"{key} spills {spill} bytes (at most {spill_ok})"
+            assert regs <= cap, f"{key} uses {regs} registers (at most {cap})"
+
+
+def test_chunked_token_kernel_fits_its_registers(tmp_path):
+    report = _ptxas_report(tmp_path, "ssu_tokens.cu")
+    for (n, st), (cap, spill_ok) in MMA_TABLE.items():
+        for i64 in (False, True):
+            key = ("ssu_tokens_mma_kernel", n, st, i64)
             assert key in report, f"{key} not compiled"
             regs, spill = report[key]
             assert spill <= spill_ok, f"{key} spills {spill} bytes (at most {spill_ok})"

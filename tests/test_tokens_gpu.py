@@ -82,19 +82,25 @@ def test_one_token_equals_ssu_update_bitwise(op):
     assert np.array_equal(got_out[:, 0], bits_of(ref["out"]))
 
 
+# Calls with intermediate states run the general kernel, calls without the rescaling one.
+WITH_INTER = pytest.mark.parametrize("with_inter", [True, False], ids=["inter", "no_inter"])
+
+
 @pytest.mark.parametrize("T", [2, 3, 4, 8])
 @pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
-def test_tokens_match_oracle(op, T, idx_dtype):
+@WITH_INTER
+def test_tokens_match_oracle(op, T, idx_dtype, with_inter):
     pr, x, dt, B, C = _tokens_problem(10, T, seed=T)
-    got = _run(op, pr, x, dt, B, C, idx_dtype=idx_dtype)
+    got = _run(op, pr, x, dt, B, C, idx_dtype=idx_dtype, with_inter=with_inter)
     assert _check_all(pr, x, dt, B, C, *got) == 0
     assert op.get_error() == (0, -1)
 
 
 @pytest.mark.parametrize("P,G", [(40, 1), (3, 2), (100, 4)])
-def test_tokens_ragged_headdim_and_groups(op, P, G):
+@WITH_INTER
+def test_tokens_ragged_headdim_and_groups(op, P, G, with_inter):
     pr, x, dt, B, C = _tokens_problem(6, 3, H=8, P=P, G=G, seed=P)
-    got = _run(op, pr, x, dt, B, C)
+    got = _run(op, pr, x, dt, B, C, with_inter=with_inter)
     _check_all(pr, x, dt, B, C, *got)
 
 
@@ -139,11 +145,14 @@ def test_tokens_strided_views(op):
     _check_all(pr, x, dt, B, C, dev["state_pool"].cpu().numpy(), bits_of(out), None)
 
 
-def test_tokens_serving_batch_128_every_request(op):
-    # batch 128, 16 heads, 3 tokens per request (one verified token plus two drafts), a
-    # 2432-slot pool: every request's state, readouts and intermediate states against the
-    # oracle (in chunks of 32 requests), untouched slots bit-identical.
-    bs, T, H = 128, 3, 16
+@pytest.mark.parametrize("T,with_inter", [(3, True), (3, False), (8, False)],
+                         ids=["3-inter", "3-no_inter", "8-no_inter"])
+def test_tokens_serving_batch_128_every_request(op, T, with_inter):
+    # batch 128, 16 heads, 3 tokens per request (one verified token plus two drafts) and 8
+    # (the bench's longest), a 2432-slot pool, the built-in launch table: every request's
+    # state, readouts and intermediate states (where asked for) against the oracle (in chunks
+    # of 32 requests), untouched slots bit-identical.
+    bs, H = 128, 16
     rng = np.random.default_rng(3)
     pool = wl.state_pool(rng, 2432, H)
     idx = wl.rotation_sets(bs, 19, seed=3)[4]
@@ -152,7 +161,7 @@ def test_tokens_serving_batch_128_every_request(op):
     x, dt, B, C = (np.stack([s[k] for s in steps], 1) for k in range(4))
     pool_d = torch.from_numpy(pool).cuda()
     out = torch.zeros(bs, T, H, 64, dtype=torch.bfloat16, device="cuda")
-    inter = torch.empty(bs, T, H, 64, 128, device="cuda")
+    inter = torch.empty(bs, T, H, 64, 128, device="cuda") if with_inter else None
     op.tokens(pool_d, torch.from_numpy(idx).cuda(), bf16_tensor(x, "cuda"), bf16_tensor(dt, "cuda"),
               torch.from_numpy(dt_bias).cuda(), torch.from_numpy(A).cuda(), bf16_tensor(B, "cuda"),
               bf16_tensor(C, "cuda"), torch.from_numpy(D).cuda(), out, inter)
@@ -166,9 +175,10 @@ def test_tokens_serving_batch_128_every_request(op):
                                                          D)
         got_pool = pool_d[torch.from_numpy(idx[rows]).cuda()].cpu().numpy()
         check_state(got_pool, ref_pool)
-        got_inter = inter[torch.from_numpy(rows).cuda()].cpu().numpy()
+        got_inter = inter[torch.from_numpy(rows).cuda()].cpu().numpy() if with_inter else None
         for t in range(T):
-            check_state(got_inter[:, t], ref_inter[:, t])
+            if with_inter:
+                check_state(got_inter[:, t], ref_inter[:, t])
             Ch, Dx = expected_terms(x[rows, t], D, C[rows, t], 1, H)
             check_y(out_bits[rows, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, 128)
     mask = np.ones(2432, bool)
@@ -178,33 +188,41 @@ def test_tokens_serving_batch_128_every_request(op):
 
 
 @pytest.mark.parametrize("idx_dtype", [torch.int32, torch.int64])
-def test_tokens_many_tiles_per_warp_with_skips(op, idx_dtype):
-    """Enough tiles that every persistent warp takes many (its shared-memory ring wraps over
-    and over), with skipped requests scattered among them: every request against the oracle,
-    the skipped ones counted and left alone."""
+@WITH_INTER
+def test_tokens_many_requests_with_skips(op, idx_dtype, with_inter):
+    """More requests than the grid's third dimension holds at once in flight, with skipped
+    requests scattered among them: every request against the oracle, the skipped ones counted
+    and left alone."""
     bs, T, H = 300, 2, 16
     pr, x, dt, B, C = _tokens_problem(bs, T, H=H, pool_size=bs + 40, seed=41)
     idx = pr.idx.copy()
     bad = [0, 7, 150, 151, 299]
     idx[bad] = [bs + 40, -1, -5, 1 << 30, bs + 41]
-    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, idx=idx, idx_dtype=idx_dtype)
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, idx=idx, idx_dtype=idx_dtype,
+                                        with_inter=with_inter)
     skipped = _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter, idx=idx)
     assert skipped == len(bad)
     assert op.get_error() == (len(bad), 0)
-    assert (got_inter[bad] == 123.0).all()
+    assert (got_out[bad] == 0).all()
+    if with_inter:
+        assert (got_inter[bad] == 123.0).all()
 
 
 @pytest.mark.parametrize("T,N", [(2, 128), (5, 128), (3, 64), (4, 256)])
-def test_unaligned_B_C_take_the_scalar_loads_with_the_same_bits(op, T, N):
+@WITH_INTER
+def test_unaligned_B_C_take_the_scalar_loads_with_the_same_bits(op, T, N, with_inter):
     """B and C one element past an 8-byte boundary (only 2-byte aligned) cannot be read as
-    column vectors; the kernel then loads them element by element.  Both forms must give the
-    same bits, at several token counts (the input ring refills on odd and even tokens)."""
+    column vectors; the kernel then loads them element by element.  With intermediate states
+    both forms run the general kernel and must give the same bits, at several token counts
+    (the input ring refills on odd and even tokens).  Without them the aligned call runs the
+    chunked kernel (dstate 64 and 128) and the unaligned one the general kernel: both against
+    the oracle."""
     bs, H = 10, 8
     pr, x, dt, B, C = _tokens_problem(bs, T, H=H, N=N, seed=T + N)
-    aligned_pool, aligned_out, aligned_inter = _run(op, pr, x, dt, B, C)
+    aligned_pool, aligned_out, aligned_inter = _run(op, pr, x, dt, B, C, with_inter=with_inter)
     dev = to_device(pr, "cuda")
     out = torch.zeros(bs, T, H, 64, dtype=torch.bfloat16, device="cuda")
-    inter = torch.full((bs, T, H, 64, N), 123.0, device="cuda")
+    inter = torch.full((bs, T, H, 64, N), 123.0, device="cuda") if with_inter else None
     # [bs, T, 1, N] views at element offset 1 of a wider buffer: 2-byte alignment only
     width = 2 * N + 3
     buf = torch.zeros(bs, T, width, dtype=torch.bfloat16, device="cuda")
@@ -216,15 +234,22 @@ def test_unaligned_B_C_take_the_scalar_loads_with_the_same_bits(op, T, N):
     op.tokens(dev["state_pool"], dev["state_batch_indices"], bf16_tensor(x, "cuda"),
               bf16_tensor(dt, "cuda"), dev["dt_bias"], dev["A"], Bv, Cv, dev["D"], out, inter)
     torch.cuda.synchronize()
-    assert np.array_equal(dev["state_pool"].cpu().numpy(), aligned_pool)
-    assert np.array_equal(bits_of(out), aligned_out)
-    assert np.array_equal(inter.cpu().numpy(), aligned_inter)
+    if with_inter or N == 256:
+        assert np.array_equal(dev["state_pool"].cpu().numpy(), aligned_pool)
+        assert np.array_equal(bits_of(out), aligned_out)
+        if with_inter:
+            assert np.array_equal(inter.cpu().numpy(), aligned_inter)
+    else:
+        _check_all(pr, x, dt, B, C, aligned_pool, aligned_out, None)
+        _check_all(pr, x, dt, B, C, dev["state_pool"].cpu().numpy(), bits_of(out), None)
 
 
-def test_long_token_runs_cross_the_per_warp_scalar_batches(op):
-    """dt and dA are computed 32 tokens at a time (one per lane); 40 tokens cross a batch."""
+@WITH_INTER
+def test_long_token_runs_cross_the_per_warp_scalar_batches(op, with_inter):
+    """dt and dA are computed 32 tokens at a time (one per lane), and a rescaled batch ends
+    there; 40 tokens cross a batch."""
     pr, x, dt, B, C = _tokens_problem(3, 40, H=4, seed=21)
-    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C)
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, with_inter=with_inter)
     _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter)
 
 
@@ -245,14 +270,15 @@ def test_one_token_with_intermediate_runs_the_token_kernel_bitwise(op):
 
 
 @pytest.mark.parametrize("N", [128, 256])
-def test_most_tokens_per_call(op, N):
+@WITH_INTER
+def test_most_tokens_per_call(op, N, with_inter):
     """The largest token count one call takes (SSU_MAX_TOKENS = 64): every token's readout and
     intermediate state against the oracle; one more token is refused before any launch."""
     pr = wl.make_problem(3, 4, 64, N, 1, pool_size=5, seed=31)
     rng = np.random.default_rng(38)
     steps = [wl.request_inputs(rng, 3, 4, 64, N, 1) for _ in range(64)]
     x, dt, B, C = (np.stack([s[i] for s in steps], 1) for i in range(4))
-    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C)
+    got_pool, got_out, got_inter = _run(op, pr, x, dt, B, C, with_inter=with_inter)
     _check_all(pr, x, dt, B, C, got_pool, got_out, got_inter)
     assert op.get_error() == (0, -1)
     steps.append(wl.request_inputs(rng, 3, 4, 64, N, 1))
@@ -260,3 +286,52 @@ def test_most_tokens_per_call(op, N):
     with pytest.raises(ssu.SsuError) as e:
         _run(op, pr, x, dt, B, C, with_inter=False)
     assert e.value.status == ssu.SSU_ERR_INVALID_ARG
+
+
+def _extreme_heads(pr, dt, kind):
+    """Per-head parameters whose decay products leave the rescaling range [2^-60, 2^60]:
+    "underflow": dt near 200, so dA = exp(dt A) is 0 in fp32 from the first token on;
+    "growth": A = +1 and every dt = softplus(2.5) = 2.58, so dA = 13.2 and the product of 17
+    tokens' dA passes 2^60 (e^43.9 > e^41.6) while the state stays finite (e^46 at most)."""
+    if kind == "underflow":
+        pr.dt_bias[:] = 200.0
+        return dt
+    pr.A[:] = 1.0
+    pr.dt_bias[:] = 2.5
+    return np.zeros_like(dt)
+
+
+@pytest.mark.parametrize("kind,T", [("underflow", 6), ("growth", 18)])
+@WITH_INTER
+def test_decay_products_outside_the_chunk_range(op, kind, T, with_inter):
+    """Decay products outside [2^-60, 2^60]: without intermediate states (and 5 tokens or more,
+    fp32 state) the chunked kernel then runs token by token (a plain update where dA itself is
+    out of range, shorter chunks where the running product leaves the range); both kernels
+    within the oracle's tolerance."""
+    pr, x, dt, B, C = _tokens_problem(6, T, H=8, seed=51 + T)
+    dt = _extreme_heads(pr, dt, kind)
+    fast_pool, fast_out, _ = _run(op, pr, x, dt, B, C, with_inter=with_inter)
+    if kind == "underflow":
+        _check_all(pr, x, dt, B, C, fast_pool, fast_out, None)
+        return
+    # Growth: the state's terms reach e^44, and an entry where they cancel keeps an fp32 error
+    # of the terms' size, so the check is relative to each slot's (and readout row's) largest
+    # value: fp32 state within 1e-5 of it, bf16 readouts within 2^-7 of it.
+    ref_pool, ref_y, _, _ = oracle.ssu_tokens(pr.pool, pr.idx, x, dt, pr.dt_bias, pr.A, B, C,
+                                              pr.D, pr.ngroups)
+    got = fast_pool[pr.idx].astype(np.float64)
+    ref = ref_pool[pr.idx]
+    scale = np.abs(ref).max(axis=(2, 3), keepdims=True)
+    assert (np.abs(got - ref) <= 1e-5 * (1 + scale)).all()
+    y = oracle.bf16_to_f64(fast_out)
+    yscale = np.abs(ref_y).max(axis=-1, keepdims=True)
+    assert (np.abs(y - ref_y) <= 2.0 ** -7 * yscale).all()
+
+
+def test_heads_in_and_out_of_the_chunk_range_in_one_call(op):
+    """Half the heads decay so fast (dA = 0) that every token of theirs takes the plain
+    update alone, the others run in chunks: every readout and state against the oracle."""
+    pr, x, dt, B, C = _tokens_problem(6, 6, H=8, seed=61)
+    pr.dt_bias[::2] = 200.0
+    got_pool, got_out, _ = _run(op, pr, x, dt, B, C, with_inter=False)
+    _check_all(pr, x, dt, B, C, got_pool, got_out, None)
