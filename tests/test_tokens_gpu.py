@@ -335,3 +335,40 @@ def test_heads_in_and_out_of_the_chunk_range_in_one_call(op):
     pr.dt_bias[::2] = 200.0
     got_pool, got_out, _ = _run(op, pr, x, dt, B, C, with_inter=False)
     _check_all(pr, x, dt, B, C, got_pool, got_out, None)
+
+
+@pytest.mark.parametrize("P,G,T", [(40, 4, 6), (96, 2, 9), (128, 1, 5), (8, 2, 7)])
+def test_chunked_kernel_headdim_groups_and_chunks(op, P, G, T):
+    """The chunked kernel (no intermediate states, fp32 state, 5 tokens or more) on head groups,
+    a headdim that ends inside a warp's 16 rows (40, 8), two 64-row slabs per head (96, 128)
+    and a second chunk (9 tokens): every readout and state against the oracle."""
+    pr, x, dt, B, C = _tokens_problem(5, T, H=8, P=P, G=G, seed=70 + P + T)
+    got = _run(op, pr, x, dt, B, C, with_inter=False)
+    assert _check_all(pr, x, dt, B, C, *got) == 0
+
+
+def test_chunked_kernel_on_packed_strided_views(op):
+    """x, B and C of 6 tokens as views into one packed [bs, T, H*P + 2N] bf16 tensor (16-byte
+    aligned, strides multiples of 8 elements), dt and the per-head operands as stride-0
+    expansions: the chunked kernel reads them in place."""
+    bs, T, H, P, N = 7, 6, 16, 64, 128
+    pr, _, _, _, _ = _tokens_problem(bs, 1, seed=23)
+    rng = np.random.default_rng(24)
+    packed = wl.f32_to_bf16_bits(rng.standard_normal((bs, T, H * P + 2 * N), dtype=np.float32))
+    dt = wl.f32_to_bf16_bits(rng.uniform(-4, 0, (bs, T, H)).astype(np.float32))
+    pk = bf16_tensor(packed, "cuda")
+    xv = pk[:, :, :H * P].view(bs, T, H, P)
+    Bv = pk[:, :, H * P:H * P + N].unsqueeze(2)
+    Cv = pk[:, :, H * P + N:].unsqueeze(2)
+    assert Bv.data_ptr() % 16 == 0 and Cv.data_ptr() % 16 == 0
+    dtv = bf16_tensor(dt, "cuda").unsqueeze(-1).expand(bs, T, H, P)
+    dev = to_device(pr, "cuda")
+    out = torch.zeros(bs, T, H, P, dtype=torch.bfloat16, device="cuda")
+    op.tokens(dev["state_pool"], dev["state_batch_indices"], xv, dtv,
+              dev["dt_bias"].unsqueeze(-1).expand(H, P), dev["A"][:, None, None].expand(H, P, N),
+              Bv, Cv, dev["D"].unsqueeze(-1).expand(H, P), out)
+    torch.cuda.synchronize()
+    x = packed[:, :, :H * P].reshape(bs, T, H, P)
+    B = packed[:, :, H * P:H * P + N].reshape(bs, T, 1, N)
+    C = packed[:, :, H * P + N:].reshape(bs, T, 1, N)
+    _check_all(pr, x, dt, B, C, dev["state_pool"].cpu().numpy(), bits_of(out), None)
