@@ -285,6 +285,17 @@ typedef struct {
  * nothing.  B and C are read as whole 4- or 8-byte column groups when their base and strides
  * allow it, element by element otherwise (same results either way).  T = 1 without an
  * intermediate buffer runs as ssu_update.
+ *
+ * Two forms compute the step.  With an intermediate buffer, with a forced launch shape, and
+ * for short runs, the tokens are applied one after another as written above.  Without an
+ * intermediate buffer, runs of 5 tokens or more on an fp32 state (16 or more on a bf16 state
+ * at dstate 128) with dstate 64 or 128, headdim a multiple of 8, and B, C and x 16-byte aligned
+ * with strides in multiples of 8 elements take the chunked matrix form: the same
+ * recurrence rewritten per chunk of up to 8 tokens through the running product of dA, on
+ * tensor-core MMAs with fp32 operands split into two tf32 parts.  Its values are the same real
+ * numbers rounded in another order: within the same tolerance of an exact evaluation, but not
+ * bit-identical to the token-by-token form.  Each form gives the same bits for the same
+ * inputs whatever the launch shape.
  */
 ssu_status_t ssu_update_tokens(ssu_handle_t handle, void *state_pool,
                                const void *state_batch_indices, const uint16_t *x,
