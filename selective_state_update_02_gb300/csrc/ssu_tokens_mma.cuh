@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(32 * kMmaWarpsPerCta, kMmaCtasPerSm)
     MmaStage<N> &st = stage[warp];
     MmaTile tl;
     tl.h = blockIdx.y;
-    tl.row0 = blockIdx.x * (kMmaWarpsPerCta * kMmaRowsPerWarp) + warp * kMmaRowsPerWarp;
+    tl.row0 = (blockIdx.x * (blockDim.x >> 5) + warp) * kMmaRowsPerWarp;  // (the launch's width)
     if (tl.row0 < p.headdim) {
         const int rA = tl.row0 + g;
         const bool liveA = rA < p.headdim, liveB = rA + 8 < p.headdim;
