@@ -146,3 +146,18 @@ def test_reference_arm_and_cpu_baseline_time_the_oracle_alike(capsys):
     ratio = line["value"] / base["value"]
     assert 0.6 < ratio < 1.6, (line["value"], base["value"])
     assert line["cpu_baseline"]["cores"] == base["cores"]
+
+
+def test_token_kernel_names_follow_the_library_rule():
+    # ssu_update_tokens: the chunked kernel without intermediates and without a forced shape,
+    # fp32 state at dstate 64 / 128 from 5 tokens, bf16 at dstate 128 from 16; else general
+    k = bench.tokens_kernel
+    assert k(5, False, 128, "f32", False) == "ssu_tokens_mma_kernel"
+    assert k(4, False, 128, "f32", False) == "ssu_tokens_kernel"
+    assert k(8, False, 64, "f32", False) == "ssu_tokens_mma_kernel"
+    assert k(8, True, 128, "f32", False) == "ssu_tokens_kernel"
+    assert k(8, False, 128, "f32", True) == "ssu_tokens_kernel"
+    assert k(8, False, 256, "f32", False) == "ssu_tokens_kernel"
+    assert k(15, False, 128, "bf16", False) == "ssu_tokens_kernel"
+    assert k(16, False, 128, "bf16", False) == "ssu_tokens_mma_kernel"
+    assert k(64, False, 64, "bf16", False) == "ssu_tokens_kernel"

@@ -96,6 +96,8 @@ CASES = [
     (3, 4, 24, 256, 1, "f32", True, False, 3),
     (70, 8, 64, 128, 1, "bf16", False, True, 0),
     (1, 2, 3, 128, 2, "f32", False, True, 1),
+    # past the 65,535 CTAs of the grid's third dimension (the staging kernel loops)
+    (70_000, 1, 16, 64, 1, "f32", False, True, 0),
 ]
 
 
