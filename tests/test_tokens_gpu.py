@@ -372,3 +372,59 @@ def test_chunked_kernel_on_packed_strided_views(op):
     B = packed[:, :, H * P:H * P + N].reshape(bs, T, 1, N)
     C = packed[:, :, H * P + N:].reshape(bs, T, 1, N)
     _check_all(pr, x, dt, B, C, dev["state_pool"].cpu().numpy(), bits_of(out), None)
+
+
+def _fuzz_cases(n=40, seed=2026):
+    """Seeded random shapes that the chunked kernel takes (no intermediate states, headdim a
+    multiple of 8): fp32 state at dstate 64 / 128 from 5 tokens, bf16 at dstate 128 from 16."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        bf16 = i % 8 == 7
+        N = 128 if bf16 else int(rng.choice([64, 128]))
+        T = int(rng.integers(16, 25)) if bf16 else int(rng.integers(5, 25))
+        H = int(rng.choice([1, 2, 3, 4, 6, 8]))
+        G = int(rng.choice([g for g in (1, 2, 3) if H % g == 0]))
+        P = int(rng.choice([8, 16, 24, 40, 64, 72, 96, 128]))
+        bs = int(rng.integers(1, 24))
+        cases.append((i, bs, T, H, G, P, N, "bf16" if bf16 else "f32", bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"case{c[0]}")
+def test_chunked_kernel_random_shapes(op, case):
+    """Every request of a random call against the oracle (shape, groups, token count across
+    chunk boundaries, index width and state type drawn from one seeded generator)."""
+    i, bs, T, H, G, P, N, sdt, i64 = case
+    pr = wl.make_problem(bs, H, P, N, G, pool_size=bs + 5, seed=1000 + i, state_dtype=sdt)
+    rng = np.random.default_rng(2000 + i)
+    steps = [wl.request_inputs(rng, bs, H, P, N, G) for _ in range(T)]
+    x, dt, B, C = (np.stack([s[k] for s in steps], 1) for k in range(4))
+    dev = to_device(pr, "cuda", torch.int64 if i64 else torch.int32)
+    out = torch.zeros(bs, T, H, P, dtype=torch.bfloat16, device="cuda")
+    op.tokens(dev["state_pool"], dev["state_batch_indices"], bf16_tensor(x, "cuda"),
+              bf16_tensor(dt, "cuda"), dev["dt_bias"], dev["A"], bf16_tensor(B, "cuda"),
+              bf16_tensor(C, "cuda"), dev["D"], out)
+    torch.cuda.synchronize()
+    widen = (lambda a: oracle.bf16_to_f64(a)) if sdt == "bf16" else (lambda a: a)
+    ref_pool, ref_y, ref_inter, _ = oracle.ssu_tokens(widen(pr.pool), pr.idx, x, dt, pr.dt_bias,
+                                                     pr.A, B, C, pr.D, G)
+    got = dev["state_pool"].cpu()
+    got = (oracle.bf16_to_f64(got.view(torch.int16).numpy().view(np.uint16)) if sdt == "bf16"
+           else got.numpy())
+    if sdt == "bf16":
+        from parity_util import ulp_bf16
+        err = np.maximum(np.abs(got[pr.idx] - ref_pool[pr.idx]) - 0.5 * ulp_bf16(ref_pool[pr.idx]),
+                         0.0) / (1.0 + np.abs(ref_pool[pr.idx]))
+        assert err.max() <= 1e-5
+    else:
+        check_state(got[pr.idx], ref_pool[pr.idx])
+    untouched = np.setdiff1d(np.arange(pr.pool.shape[0]), pr.idx)
+    assert np.array_equal(dev["state_pool"].cpu().numpy()[untouched] if sdt == "f32"
+                          else dev["state_pool"].cpu().view(torch.int16).numpy()[untouched],
+                          pr.pool[untouched] if sdt == "f32" else pr.pool[untouched].view(np.int16))
+    out_bits = bits_of(out)
+    for t in range(T):
+        Ch, Dx = expected_terms(x[:, t], pr.D, C[:, t], G, H)
+        check_y(out_bits[:, t], ref_y[:, t], ref_inter[:, t], Ch, Dx, N, f"y token {t}")
+    assert op.get_error() == (0, -1)
